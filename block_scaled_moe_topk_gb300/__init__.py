@@ -1,0 +1,183 @@
+"""GB300-native block-scaled MoE top-k expert layer (A8W4 / A4W4).
+
+A thin ctypes binding over ``libmoe_topk.so`` (the C ABI declared in
+``include/moe_topk.h``).  Every function here only marshals torch tensors to
+device pointers and sizes and raises on a non-zero status; every step of the
+layer runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing the functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "lib", "moe_status_string", "moe_workspace_bytes",
+    "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_quantize_mx", "moe_a8w4_forward",
+    "moe_a4w4_forward", "moe_read_device_status", "moe_forward_launch_count", "workspace_views",
+]
+
+MOE_ACT_MXFP8 = 0
+MOE_ACT_MXFP4 = 1
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_topk.so")
+
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_UNSUPPORTED_DEVICE",
+    4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_MISALIGNED",
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "status", "topk_ids", "topk_w", "counts", "offsets", "padded_offsets", "mtile_base", "chunk_hist",
+        "sorted_pair", "inv", "inv_padded", "xq", "xs", "a2", "a2s", "y2", "total")] + [
+        ("rows_cap", ctypes.c_int64), ("nchunk", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe_topk.so (built in-tree by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no non-CUDA fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_status_string.argtypes = [i32]
+    L.moe_get_workspace_layout.restype = i32
+    L.moe_get_workspace_layout.argtypes = [i64, i32, i32, i32, i32, i32, ctypes.POINTER(WorkspaceLayout)]
+    L.moe_workspace_bytes.restype = sz
+    L.moe_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    L.moe_topk_route.restype = i32
+    L.moe_topk_route.argtypes = [P, i64, i32, i32, P, P, P]
+    L.moe_sort_by_expert.restype = i32
+    L.moe_sort_by_expert.argtypes = [P, i64, i32, i32, P, P, P, P, P, sz, P]
+    L.moe_quantize_mx.restype = i32
+    L.moe_quantize_mx.argtypes = [P, i64, i32, i32, P, P, P]
+    for name in ("moe_a8w4_forward", "moe_a4w4_forward"):
+        f = getattr(L, name)
+        f.restype = i32
+        f.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P]
+    L.moe_read_device_status.restype = i32
+    L.moe_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
+    L.moe_forward_launch_count.restype = i32
+    L.moe_forward_launch_count.argtypes = [i64]
+    _lib = L
+    return L
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoeError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def moe_get_workspace_layout(T, H, I, E, k, fmt=MOE_ACT_MXFP8) -> WorkspaceLayout:
+    lay = WorkspaceLayout()
+    _check(lib().moe_get_workspace_layout(int(T), int(H), int(I), int(E), int(k), int(fmt), ctypes.byref(lay)),
+           "moe_get_workspace_layout")
+    return lay
+
+
+def moe_workspace_bytes(T, H, I, E, k, fmt=MOE_ACT_MXFP8) -> int:
+    return int(lib().moe_workspace_bytes(int(T), int(H), int(I), int(E), int(k), int(fmt)))
+
+
+def moe_forward_launch_count(T) -> int:
+    return int(lib().moe_forward_launch_count(int(T)))
+
+
+def moe_topk_route(gate_logits, k, topk_ids, topk_w, stream=None):
+    """gate_logits fp32 [T, E] -> topk_ids int32 [T, k], topk_w fp32 [T, k] (outputs given)."""
+    T, E = gate_logits.shape
+    _check(lib().moe_topk_route(_p(gate_logits), T, E, int(k), _p(topk_ids), _p(topk_w), _stream(stream)),
+           "moe_topk_route")
+
+
+def moe_sort_by_expert(topk_ids, E, counts, offsets, sorted_pair, inv, workspace, stream=None):
+    T, k = topk_ids.shape
+    _check(lib().moe_sort_by_expert(_p(topk_ids), T, int(E), k, _p(counts), _p(offsets), _p(sorted_pair), _p(inv),
+                                    _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_sort_by_expert")
+
+
+def moe_quantize_mx(x, fmt, codes, scales, stream=None):
+    rows, K = x.shape
+    _check(lib().moe_quantize_mx(_p(x), rows, K, int(fmt), _p(codes), _p(scales), _stream(stream)),
+           "moe_quantize_mx")
+
+
+def _forward(name, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream):
+    T, H = x.shape
+    I = w2.shape[-1] * 2
+    f = getattr(lib(), name)
+    _check(f(_p(x), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale), _p(out), T, H, I, int(E), int(k),
+             _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)), name)
+
+
+def moe_a8w4_forward(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None):
+    """x bf16 [T, H], gate_logits fp32 [T, E], w1 u8 [E, 2I, H/2], w1_scale u8 [E, 2I, H/32],
+    w2 u8 [E, H, I/2], w2_scale u8 [E, H, I/32] -> out bf16 [T, H]."""
+    _forward("moe_a8w4_forward", x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream)
+
+
+def moe_a4w4_forward(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None):
+    _forward("moe_a4w4_forward", x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream)
+
+
+def moe_read_device_status(workspace, stream=None) -> int:
+    st = ctypes.c_int(0)
+    _check(lib().moe_read_device_status(_p(workspace), _stream(stream), ctypes.byref(st)), "moe_read_device_status")
+    return int(st.value)
+
+
+def workspace_views(workspace, T, H, I, E, k, fmt=MOE_ACT_MXFP8):
+    """Typed views of the forward's intermediates inside a uint8 workspace tensor."""
+    L = moe_get_workspace_layout(T, H, I, E, k, fmt)
+    R = T * k
+    hb = H if fmt == MOE_ACT_MXFP8 else H // 2
+    ib = I if fmt == MOE_ACT_MXFP8 else I // 2
+    rc = L.rows_cap
+
+    def v(off, n, dtype):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return workspace[off:off + nbytes].view(dtype)
+
+    return dict(
+        layout=L,
+        topk_ids=v(L.topk_ids, R, torch.int32).view(T, k), topk_w=v(L.topk_w, R, torch.float32).view(T, k),
+        counts=v(L.counts, E, torch.int32), offsets=v(L.offsets, E + 1, torch.int64),
+        padded_offsets=v(L.padded_offsets, E + 1, torch.int64), mtile_base=v(L.mtile_base, E + 1, torch.int32),
+        sorted_pair=v(L.sorted_pair, R, torch.int32), inv=v(L.inv, R, torch.int32),
+        inv_padded=v(L.inv_padded, R, torch.int32), xq=v(L.xq, rc * hb, torch.uint8).view(rc, hb),
+        xs=v(L.xs, rc * H // 32, torch.uint8), a2=v(L.a2, rc * ib, torch.uint8).view(rc, ib),
+        a2s=v(L.a2s, rc * I // 32, torch.uint8), y2=v(L.y2, rc * H, torch.float32).view(rc, H),
+        status=v(L.status, 8, torch.int32))

@@ -1,0 +1,474 @@
+// gemm.cu -- grouped block-scaled GEMMs of the expert layer on the tcgen05 tensor cores.
+//
+// One persistent kernel, two epilogues:
+//   GEMM1 (EPI=0): acc[r, n] = sum_K xq[r, K] * W1[e, n, K], n in [0, 2I) with rows 2j = gate_j,
+//                  2j+1 = up_j ("feat(moe): FlyDSL MegaMoE fused EP-MoE integration", description:
+//                  INTERLEAVE(g1u1)); the epilogue forms h_j = silu(gate_j) * up_j and requantises
+//                  h to MX (A2: "add A4W4 and FP8 P2P transport support to MegaMoE", Technical
+//                  Details: "emit FP4 A2 activations/scales"; E4M3 codes for A8W4).
+//   GEMM2 (EPI=1): y2[r, n] = sum_I a2[r, I] * W2[e, n, I], stored as fp32 rows.
+//
+// Tiles are 128 routed rows (one expert's padded segment) x 256 output columns.  Per CTA:
+//   warp 0      producer: TMA (activation tile 128x128B, weight tile 256x128B), a bulk copy of
+//               the activation scales (already in the 128x4 tile layout) and 4-byte cp.async
+//               copies that rearrange the canonical weight scales into that layout;
+//   warp 1      TMEM owner and MMA issuer (one thread): tcgen05.cp of the scales to TMEM, then
+//               tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1, scale_vec 1X) or kind::mxf4 (E2M1 x E2M1,
+//               scale_vec 2X) into a 128x256 fp32 accumulator in TMEM;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one routed row) per
+//               thread.
+// A 4-deep shared-memory ring with full/empty mbarriers overlaps the weight stream with the
+// MMAs.  Every wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
+// status word, lets its own copies and MMAs drain (again bounded), frees TMEM and returns.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "mx_device.cuh"
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kABytes = kRowTile * 128;   // 128 rows x 128 bytes
+constexpr int kBBytes = kNTile * 128;     // 256 rows x 128 bytes (shared-memory footprint)
+constexpr int kSfaOff = kABytes + kBBytes;
+constexpr int kSfbOff = kSfaOff + 1024;
+constexpr int kStageBytes = kSfbOff + 2048;  // 51 KiB, a multiple of 1024
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers/flags + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256;   // accumulator uses columns [0, 256)
+constexpr uint32_t kSfSlotCols = 32;
+
+struct GemmParams {  // 64-byte aligned through its CUtensorMap members
+  CUtensorMap tmap_act;
+  CUtensorMap tmap_w;
+  const uint8_t* act_sf;
+  const uint8_t* w_sf;
+  const int32_t* counts;
+  const int64_t* padded_offsets;
+  const int32_t* mtile_base;
+  uint8_t* out_codes;
+  uint8_t* out_sf;
+  float* out_f32;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int E, N, K;
+};
+
+template <int ACT>
+struct ActTraits;
+template <>
+struct ActTraits<0> {                  // E4M3 activations x E2M1 weights
+  static constexpr int kKPerStage = 128;
+  static constexpr int kMmaK = 32;
+  // The weight tile lands with an 8-byte gap after every 8 bytes of codes (32 KiB of shared
+  // memory) but its transaction count is the 16 KiB of packed codes read from global memory.
+  static constexpr int kBTxBytes = kNTile * 64;
+  static constexpr uint32_t kIdescFmt = (0u << 7) | (5u << 10);
+};
+template <>
+struct ActTraits<1> {                  // E2M1 x E2M1, packed
+  static constexpr int kKPerStage = 256;
+  static constexpr int kMmaK = 64;
+  static constexpr int kBTxBytes = kNTile * 128;
+  static constexpr uint32_t kIdescFmt = (1u << 7) | (1u << 10);
+};
+
+// Block-scaled instruction descriptor: formats, N>>3 at [17,23), E8M0 scales (bit 23),
+// M>>4 at [24,29); K-major A and B; scale-factor byte ids at [29,31) (A) and [4,6) (B).
+template <int ACT>
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
+  return ActTraits<ACT>::kIdescFmt | ((uint32_t)(kNTile >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(kRowTile >> 4) << 24) | (sf_id << 29) | (sf_id << 4);
+}
+
+struct Tile {
+  int e, mt, nt;
+};
+
+// Tiles of expert e occupy [mtile_base[e]*NT, mtile_base[e+1]*NT); inside an expert the
+// M tile is the fastest index so CTAs running side by side share the weight tile in L2.
+__device__ __forceinline__ Tile decode_tile(int64_t tile, const int32_t* mtile_base, int E, int NT) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)mtile_base[mid] * NT <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  const int mt_e = mtile_base[lo + 1] - mtile_base[lo];
+  const int64_t local = tile - (int64_t)mtile_base[lo] * NT;
+  Tile t;
+  t.e = lo;
+  t.nt = (int)(local / mt_e);
+  t.mt = (int)(local % mt_e);
+  return t;
+}
+
+struct Sync {
+  volatile int* abort_flag;
+  uint32_t* status;  // status[0]: status bits; status[1..6]: first expired wait (see below)
+  uint64_t timeout_ns;
+  uint32_t bar0;
+};
+
+// Poll a phase of an mbarrier until it completes, the CTA aborts, or the time limit passes.
+__device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*s.abort_flag) return false;
+      const uint64_t dt = global_timer_ns() - t0;
+      if (dt > limit_ns) {
+        *s.abort_flag = 1;
+        atomicOr(s.status, kStatusTimeout);
+        // first expiry only: barrier index, parity, CTA, warp, microseconds waited
+        if (atomicCAS(s.status + 1, 0u, 1u) == 0u) {
+          s.status[2] = (bar - s.bar0) / 8;
+          s.status[3] = parity;
+          s.status[4] = blockIdx.x;
+          s.status[5] = threadIdx.x / 32;
+          s.status[6] = (uint32_t)(dt / 1000);
+        }
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform form: every lane polls, and the warp proceeds only if all lanes saw the
+// phase complete, so no lane can run ahead into a .sync.aligned tcgen05 instruction
+// while another one is leaving on the abort path.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns) {
+  const bool ok = bounded_wait(bar, parity, s, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdiv_rn(g, 1.0f + expf(-g)) * u; }
+
+template <int ACT, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using TR = ActTraits<ACT>;
+  constexpr int kMmaPerStage = TR::kKPerStage / TR::kMmaK;  // 4
+  constexpr int kAtomsPerStage = TR::kKPerStage / 128;      // k-atoms of 4 scale blocks
+  constexpr uint32_t kSfaCols = kAtomsPerStage * 4;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kBarOff;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t tmem_full_bar = bar0 + 8u * (2 * kStages);
+  const uint32_t tmem_empty_bar = tmem_full_bar + 8;
+  const uint32_t drain_bar = tmem_full_bar + 16;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * (2 * kStages + 3));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1 + 32);  // producer's expect_tx arrive + 32 cp.async arrivals
+      mbar_init(empty_bar(s), 1);      // tcgen05.commit
+    }
+    mbar_init(tmem_full_bar, 1);
+    mbar_init(tmem_empty_bar, 4);      // one arrival per epilogue warp
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const Sync sync{abort_flag, p.status, p.timeout_ns, bar0};
+  const int NT = p.N / kNTile;
+  const int K = p.K;
+  const int nks = (K + TR::kKPerStage - 1) / TR::kKPerStage;
+  const int64_t total_tiles = (int64_t)p.mtile_base[p.E] * NT;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    int slot = 0;
+    uint32_t phase = 0;
+    int armed_parity[kStages];
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const Tile tc = decode_tile(tile, p.mtile_base, p.E, NT);
+      const int64_t row0 = p.padded_offsets[tc.e] + (int64_t)tc.mt * kRowTile;
+      const int n0 = tc.nt * kNTile;
+      const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!warp_wait(empty_bar(slot), phase ^ 1u, sync, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const int katoms = min(TR::kKPerStage, K - ks * TR::kKPerStage) / 128;
+        const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(kABytes + TR::kBTxBytes + katoms * 512));
+          tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
+          tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
+          bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
+                    (uint32_t)katoms * 512u, full_bar(slot));
+        }
+        for (int item = lane; item < kNTile * katoms; item += 32) {
+          const int r = item & (kNTile - 1), ka = item / kNTile;
+          const uint8_t* src = wsf_rows + (int64_t)r * (K / 32) + ks * (TR::kKPerStage / 32) + ka * 4;
+          const uint32_t dst = st + kSfbOff + ka * 1024 + (r >> 7) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+          cp_async_4(dst, src);
+        }
+        cp_async_arrive_noinc(full_bar(slot));
+        armed_parity[slot] = (int)phase;
+        if (++slot == kStages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // Let every copy this warp started land before the CTA can exit.
+    cp_async_wait_all();
+    for (int s = 0; s < kStages; ++s)
+      if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    int slot = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued = false;
+    for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      if (!warp_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!warp_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int kvalid = min(TR::kKPerStage, K - ks * TR::kKPerStage);
+        const int katoms = kvalid / 128;
+        const int nmma = kvalid / TR::kMmaK;
+        if (lane == 0) {
+          fence_proxy_async_smem();  // scales written by cp.async, read by tcgen05.cp
+          const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
+          const uint32_t sf_col = tmem_base + kSfCol0 + (uint32_t)slot * kSfSlotCols;
+          for (int ka = 0; ka < katoms; ++ka) {
+            tc_cp_32x128b_warpx4(sf_col + ka * 4, smem_desc(st + kSfaOff + ka * 512, 128, 128, kLayoutNone));
+#pragma unroll
+            for (int na = 0; na < 2; ++na)
+              tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8 + na * 4,
+                                   smem_desc(st + kSfbOff + ka * 1024 + na * 512, 128, 128, kLayoutNone));
+          }
+#pragma unroll
+          for (int j = 0; j < kMmaPerStage; ++j) {
+            if (j < nmma) {
+              const uint64_t adesc = smem_desc(st + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bdesc = smem_desc(st + kABytes + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const int kblk = j * TR::kMmaK / 32;  // first 32-block of this MMA inside the stage
+              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3));
+              const uint32_t sfa = sf_col + (kblk >> 2) * 4;
+              const uint32_t sfb = sf_col + kSfaCols + (kblk >> 2) * 8;
+              const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
+              if (ACT == 0) tc_mma_mxf8f6f4(tmem_base, adesc, bdesc, idesc, sfa, sfb, acc);
+              else tc_mma_mxf4(tmem_base, adesc, bdesc, idesc, sfa, sfb, acc);
+            }
+          }
+          tc_commit(empty_bar(slot));
+          issued = true;
+        }
+        __syncwarp();
+        if (++slot == kStages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(tmem_full_bar);
+      __syncwarp();
+      acc_phase ^= 1u;
+    }
+    // Make sure no MMA or TMEM copy of this CTA is still running before TMEM is freed.
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    if (issued) {
+      if (lane == 0) tc_commit(drain_bar);
+      __syncwarp();
+      warp_wait(drain_bar, 0, sync, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may read
+    uint32_t acc_phase = 0;
+    for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile tc = decode_tile(tile, p.mtile_base, p.E, NT);
+      const int row_local = tc.mt * kRowTile + quad * 32 + lane;
+      const bool valid = row_local < p.counts[tc.e];
+      const int64_t prow = p.padded_offsets[tc.e] + row_local;
+      if (!warp_wait(tmem_full_bar, acc_phase, sync, p.timeout_ns)) break;
+      tc_fence_after();
+      const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16);
+      if (EPI == 0) {
+        const int I = p.N / 2;
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+          float acc[64];
+          tc_ld_32x32b_x32(trow + blk * 64, acc);
+          tc_ld_32x32b_x32(trow + blk * 64 + 32, acc + 32);
+          tc_wait_ld();
+          float h[32];
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            h[i] = silu_mul(acc[2 * i], acc[2 * i + 1]);
+            amax = fmaxf(amax, fabsf(h[i]));
+          }
+          const MxScale sc = mx_scale<ACT>(amax);
+          const int kb = tc.nt * 4 + blk;  // 32-wide block of h
+          if (valid) {
+            if (ACT == 0) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out_codes + prow * I + kb * 32);
+              const uint2 c0 = pack_e4m3x8(h, sc.mult), c1 = pack_e4m3x8(h + 8, sc.mult);
+              const uint2 c2 = pack_e4m3x8(h + 16, sc.mult), c3 = pack_e4m3x8(h + 24, sc.mult);
+              dst[0] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+              dst[1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(p.out_codes + prow * (I / 2) + kb * 16);
+              *dst = make_uint4(pack_e2m1x8(h, sc.mult), pack_e2m1x8(h + 8, sc.mult), pack_e2m1x8(h + 16, sc.mult),
+                                pack_e2m1x8(h + 24, sc.mult));
+            }
+            p.out_sf[sf_tile_offset(prow, kb, I)] = sc.byte;
+          }
+        }
+      } else {
+        float* dst_row = p.out_f32 + prow * p.N + tc.nt * kNTile;
+#pragma unroll 1
+        for (int c = 0; c < kNTile / 32; ++c) {
+          float v[32];
+          tc_ld_32x32b_x32(trow + c * 32, v);
+          tc_wait_ld();
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst_row + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty_bar);
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+template <int ACT, int EPI>
+cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !attr_set[dev]) {
+    err = cudaFuncSetAttribute(moe_gemm_kernel<ACT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
+  EncodeTiledFn encode = get_encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  const int K = a.K;
+  const uint64_t act_row_bytes = ACT == 0 ? (uint64_t)K : (uint64_t)K / 2;
+  {
+    const cuuint64_t dims[2] = {act_row_bytes, (cuuint64_t)a.rows_cap};
+    const cuuint64_t strides[1] = {act_row_bytes};
+    const cuuint32_t box[2] = {128, (cuuint32_t)kRowTile};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&p.tmap_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.act), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t row_bytes = (uint64_t)K / 2;
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * (uint64_t)a.N};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kNTile, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r;
+    if (ACT == 0) {  // packed FP4 in global, 8-byte gap after every 16 codes in shared memory
+      const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)a.N, (cuuint64_t)a.E};
+      r = encode(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(a.w), dims, strides, box,
+                 es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {  // packed FP4 kept packed
+      const cuuint64_t dims[3] = {row_bytes, (cuuint64_t)a.N, (cuuint64_t)a.E};
+      r = encode(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.w), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  p.act_sf = a.act_sf;
+  p.w_sf = a.w_sf;
+  p.counts = a.counts;
+  p.padded_offsets = a.padded_offsets;
+  p.mtile_base = a.mtile_base;
+  p.out_codes = a.out_codes;
+  p.out_sf = a.out_sf;
+  p.out_f32 = a.out_f32;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  p.E = a.E;
+  p.N = a.N;
+  p.K = a.K;
+  const int64_t grid = std::min<int64_t>(a.num_sms, a.max_tiles);
+  if (grid <= 0) return cudaSuccess;
+  moe_gemm_kernel<ACT, EPI><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
+  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0>(a, s) : launch_typed<0, 1>(a, s);
+  return a.epilogue == 0 ? launch_typed<1, 0>(a, s) : launch_typed<1, 1>(a, s);
+}
+
+}  // namespace moe

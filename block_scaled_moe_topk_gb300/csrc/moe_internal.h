@@ -1,0 +1,107 @@
+// moe_internal.h -- launchers shared between the host API and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+// Routing chunk: tokens handled by one routing block (its expert histogram is one
+// column of chunk_hist).
+constexpr int kTokensPerChunk = 256;
+constexpr int kRowTile = 128;   // rows per GEMM M tile; expert segments are padded to it
+constexpr int kNTile = 256;     // output columns per GEMM N tile
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 8;
+
+// Device status word bits (the host maps them to moe_status_t).
+constexpr uint32_t kStatusInvalidArg = 1u;  // an expert id outside [0, E)
+constexpr uint32_t kStatusTimeout = 2u;     // a bounded in-kernel wait expired
+
+struct RouteArgs {
+  const float* logits;  // [T, E]
+  int64_t T;
+  int E, k;
+  int32_t* ids;         // [T, k]
+  float* w;             // [T, k]
+  int32_t* chunk_hist;  // [E, nchunk] or null
+  int64_t nchunk;
+  uint32_t* status;     // reset to 0 by block 0 when reset_status
+  int reset_status;
+};
+
+struct SortArgs {
+  const int32_t* ids;  // [T*k]
+  int64_t T;
+  int E, k;
+  int32_t* chunk_hist;       // [E, nchunk]: histogram in, exclusive per-expert chunk base out
+  int64_t nchunk;
+  int32_t* counts;           // [E]
+  int64_t* offsets;          // [E+1]
+  int64_t* padded_offsets;   // [E+1] or null
+  int32_t* mtile_base;       // [E+1] or null
+  int32_t* sorted_pair;      // [T*k]
+  int32_t* inv;              // [T*k]
+  int32_t* inv_padded;       // [T*k] or null
+  uint32_t* status;
+};
+
+// route.cu
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+// Histogram of externally supplied ids (standalone sort entry point).
+cudaError_t launch_histogram(const SortArgs& a, cudaStream_t s);
+// sort.cu: per-expert chunk bases + offsets, then the stable scatter.
+cudaError_t launch_sort(const SortArgs& a, cudaStream_t s);
+
+// quant.cu
+struct QuantArgs {
+  const uint16_t* x;      // bf16 [rows, K]
+  int64_t rows;
+  int K;
+  int fmt;                // 0 = E4M3, 1 = E2M1
+  uint8_t* codes;
+  uint8_t* scales;
+  // Permuted mode (forward): row t goes to rows inv_padded[t*k + j], j < k, and
+  // its scales to the 128x4 tile layout.  Canonical mode when inv_padded == null.
+  const int32_t* inv_padded;
+  int k;
+};
+cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
+
+// gemm.cu
+struct GemmArgs {
+  int act_fmt;            // 0: E4M3 activations (kind::mxf8f6f4), 1: E2M1 (kind::mxf4)
+  int epilogue;           // 0: SwiGLU + MX requant (GEMM1), 1: fp32 rows (GEMM2)
+  const uint8_t* act;     // activation codes [rows_cap, K or K/2]
+  const uint8_t* act_sf;  // [rows_cap/128][K/128][512]
+  int64_t rows_cap;
+  const uint8_t* w;       // MXFP4 [E, N, K/2]
+  const uint8_t* w_sf;    // E8M0 [E, N, K/32]
+  int E, N, K;
+  const int32_t* counts;
+  const int64_t* padded_offsets;
+  const int32_t* mtile_base;
+  int64_t max_tiles;      // host upper bound on tiles (grid sizing)
+  uint8_t* out_codes;     // GEMM1: A2 codes [rows_cap, N/2 or N/4]
+  uint8_t* out_sf;        // GEMM1: A2 scales, 128x4 tile layout over N/2 columns
+  float* out_f32;         // GEMM2: y2 [rows_cap, N]
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int num_sms;
+};
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+// combine.cu
+struct CombineArgs {
+  const float* y2;          // [rows_cap, H]
+  const float* w;           // [T, k]
+  const int32_t* inv_padded;
+  int64_t T;
+  int H, k;
+  uint16_t* out;            // bf16 [T, H]
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+}  // namespace moe

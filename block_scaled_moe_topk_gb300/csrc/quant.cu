@@ -1,0 +1,96 @@
+// quant.cu -- BF16 -> MXFP8 (E4M3) / MXFP4 (E2M1) quantisation with one E8M0 scale
+// per 1x32 block ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical
+// Details; OCP Microscaling v1.0 scale rule s = floor(log2 amax) - emax + 127).
+//
+// Each thread owns 8 consecutive elements (one 16-byte load); four threads form a
+// 32-element block and agree on its amax with two shuffles.  In the forward the
+// codes of token t are written straight to its k padded expert rows
+// inv_padded[t*k + j] (the permute is fused here), and the scales go to the
+// 128x4 tile layout that the GEMM's tensor-memory scale copy reads.
+#include <cuda_bf16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "mx_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kQuantThreads = 256;
+constexpr int kColsPerBlock = kQuantThreads * 8;
+
+template <int FMT>
+__global__ void __launch_bounds__(kQuantThreads) quant_kernel(QuantArgs a) {
+  const int K = a.K;
+  const int col_blocks = (K + kColsPerBlock - 1) / kColsPerBlock;
+  const int64_t work = a.rows * col_blocks;
+  for (int64_t wi = blockIdx.x; wi < work; wi += gridDim.x) {
+    const int64_t row = wi / col_blocks;
+    const int col0 = (int)(wi % col_blocks) * kColsPerBlock + threadIdx.x * 8;
+    const bool active = col0 < K;
+    float v[8];
+    if (active) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(a.x + row * K + col0);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (!active) continue;  // whole 4-lane groups are active or not (K % 32 == 0)
+    const MxScale sc = mx_scale<FMT>(amax);
+    const int kb = col0 / 32;
+    const bool scale_writer = (threadIdx.x & 3) == 0;
+    if (FMT == 0) {
+      const uint2 codes = pack_e4m3x8(v, sc.mult);
+      if (a.inv_padded == nullptr) {
+        *reinterpret_cast<uint2*>(a.codes + row * K + col0) = codes;
+        if (scale_writer) a.scales[row * (K / 32) + kb] = sc.byte;
+      } else {
+        for (int j = 0; j < a.k; ++j) {
+          const int64_t prow = a.inv_padded[row * a.k + j];
+          *reinterpret_cast<uint2*>(a.codes + prow * K + col0) = codes;
+          if (scale_writer) a.scales[sf_tile_offset(prow, kb, K)] = sc.byte;
+        }
+      }
+    } else {
+      const uint32_t codes = pack_e2m1x8(v, sc.mult);
+      if (a.inv_padded == nullptr) {
+        *reinterpret_cast<uint32_t*>(a.codes + row * (K / 2) + col0 / 2) = codes;
+        if (scale_writer) a.scales[row * (K / 32) + kb] = sc.byte;
+      } else {
+        for (int j = 0; j < a.k; ++j) {
+          const int64_t prow = a.inv_padded[row * a.k + j];
+          *reinterpret_cast<uint32_t*>(a.codes + prow * (K / 2) + col0 / 2) = codes;
+          if (scale_writer) a.scales[sf_tile_offset(prow, kb, K)] = sc.byte;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
+  const int col_blocks = (a.K + kColsPerBlock - 1) / kColsPerBlock;
+  const int64_t work = a.rows * col_blocks;
+  if (work == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<int64_t>(work, 152 * 16);
+  if (a.fmt == 0) quant_kernel<0><<<grid, kQuantThreads, 0, s>>>(a);
+  else quant_kernel<1><<<grid, kQuantThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

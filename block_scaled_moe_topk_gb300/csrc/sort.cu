@@ -1,0 +1,137 @@
+// sort.cu -- deterministic, stable sort of the routed (token, slot) pairs by expert.
+//
+// The local form of the dispatch step of "feat(moe): FlyDSL MegaMoE fused EP-MoE
+// integration" (description: dispatch+gemm1+quant+gemm2+combine).  Offsets are
+// 64-bit: the same page reports an int32 kernel argument overflowing above 8192
+// batched tokens per rank.
+//
+// Three phases, no atomics on the output order:
+//   1. per-chunk expert histograms (route.cu, fused into the routing kernel);
+//   2. one block: per-expert exclusive prefix over chunks, then prefixes over
+//      experts -> counts, offsets, 128-row padded offsets, M-tile bases;
+//   3. one warp per chunk walks its pairs in order and places each at
+//      offset[e] + chunk_base[e] + rank, so equal experts keep pair order.
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+template <typename T>
+__device__ __forceinline__ T warp_inclusive_scan(T v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const T o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+
+// Exclusive block-wide prefix of one int64 value per thread (kScanThreads threads).
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t* warp_tot, int64_t* total) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int64_t incl = warp_inclusive_scan<int64_t>(v, lane);
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int64_t wv = warp_tot[lane];
+    const int64_t wincl = warp_inclusive_scan<int64_t>(wv, lane);
+    warp_tot[lane] = wincl - wv;
+    if (lane == 31) *total = wincl;
+  }
+  __syncthreads();
+  const int64_t r = warp_tot[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(SortArgs a) {
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int64_t warp_tot[32];
+  __shared__ int64_t total;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int E = a.E;
+  const int64_t nchunk = a.nchunk;
+  // per expert: exclusive prefix over chunks, in place
+  for (int e = warp; e < E; e += kScanThreads / 32) {
+    int32_t* col = a.chunk_hist + (int64_t)e * nchunk;
+    int running = 0;
+    for (int64_t b0 = 0; b0 < nchunk; b0 += 32) {
+      const int64_t b = b0 + lane;
+      const int v = (b < nchunk) ? col[b] : 0;
+      const int incl = warp_inclusive_scan<int>(v, lane);
+      if (b < nchunk) col[b] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) cnt[e] = running;
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int c = (e < E) ? cnt[e] : 0;
+  const int64_t off = block_exclusive_scan(c, warp_tot, &total);
+  const int64_t tot_rows = total;
+  const int64_t padded = ((int64_t)c + kRowTile - 1) / kRowTile * kRowTile;
+  const int64_t poff = block_exclusive_scan(padded, warp_tot, &total);
+  const int64_t tot_padded = total;
+  const int64_t tiles = padded / kRowTile;
+  const int64_t toff = block_exclusive_scan(tiles, warp_tot, &total);
+  const int64_t tot_tiles = total;
+  if (e < E) {
+    a.counts[e] = c;
+    a.offsets[e] = off;
+    if (a.padded_offsets) a.padded_offsets[e] = poff;
+    if (a.mtile_base) a.mtile_base[e] = (int32_t)toff;
+  }
+  if (e == 0) {
+    a.offsets[E] = tot_rows;
+    if (a.padded_offsets) a.padded_offsets[E] = tot_padded;
+    if (a.mtile_base) a.mtile_base[E] = (int32_t)tot_tiles;
+  }
+}
+
+__global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
+  __shared__ int next[kMaxExperts];
+  const int lane = threadIdx.x;
+  const int E = a.E, k = a.k;
+  const int64_t b = blockIdx.x;
+  for (int e = lane; e < E; e += 32) next[e] = a.chunk_hist[(int64_t)e * a.nchunk + b];
+  __syncwarp();
+  const int64_t q_begin = b * kTokensPerChunk * k;
+  const int64_t q_lim = q_begin + (int64_t)kTokensPerChunk * k;
+  const int64_t q_end = (a.T * k < q_lim) ? a.T * k : q_lim;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int64_t q0 = q_begin; q0 < q_end; q0 += 32) {
+    const int64_t q = q0 + lane;
+    int id = (q < q_end) ? a.ids[q] : -1;
+    const bool valid = id >= 0 && id < E;
+    if (!valid) id = -1 - lane;  // a group of its own
+    const uint32_t peers = __match_any_sync(0xffffffffu, id);
+    const int rank = __popc(peers & lt_mask);
+    const int leader = __ffs(peers) - 1;
+    int base = valid ? next[id] : 0;
+    __syncwarp();
+    if (valid && lane == leader) next[id] = base + __popc(peers);
+    __syncwarp();
+    if (valid) {
+      const int64_t local = (int64_t)base + rank;
+      const int64_t r = a.offsets[id] + local;
+      a.sorted_pair[r] = (int32_t)q;
+      a.inv[q] = (int32_t)r;
+      if (a.inv_padded) a.inv_padded[q] = (int32_t)(a.padded_offsets[id] + local);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sort(const SortArgs& a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  scan_kernel<<<1, kScanThreads, 0, s>>>(a);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  scatter_kernel<<<(unsigned)a.nchunk, 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

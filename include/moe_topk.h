@@ -1,0 +1,212 @@
+/*
+ * moe_topk.h -- C ABI of the GB300 (sm_103a) block-scaled MoE top-k expert layer.
+ *
+ * The layer (all steps run in this library's CUDA kernels, on the caller's stream):
+ *   1. top-k softmax gating over E experts;
+ *   2. a stable sort of the T*k (token, slot) pairs by expert, 64-bit offsets;
+ *   3. BF16 -> MXFP8 (E4M3) or MXFP4 (E2M1) activation quantisation, one E8M0
+ *      scale per 1x32 block;
+ *   4. grouped GEMM1 against gate/up-interleaved MXFP4 weights on the tcgen05
+ *      block-scaled tensor cores, with SwiGLU and the requantisation of the
+ *      intermediate activation (A2) fused into its epilogue;
+ *   5. grouped GEMM2 against MXFP4 weights;
+ *   6. the top-k-weighted FP32 combine back to token order, rounded to BF16.
+ *
+ * Sources for the operation (page titles and sections):
+ *   - "feat(moe): FlyDSL MegaMoE fused EP-MoE integration" (ATOM PR #1666),
+ *     description: the expert step is dispatch+gemm1+quant+gemm2+combine;
+ *     w1 gate/up rows are INTERLEAVE(g1u1) (row 2j gate_j, row 2j+1 up_j);
+ *     the expert count is passed explicitly, never inferred from weight shapes;
+ *     per-layer weight pointers are swapped per call; the forward must be
+ *     CUDA-graph capturable; more than 8192 batched tokens overflowed an int32
+ *     kernel argument (hence 64-bit offsets here).
+ *   - "add A4W4 and FP8 P2P transport support to MegaMoE" (FlyDSL PR #972),
+ *     Technical Details: BF16 activations quantised with per-1x32 E8M0 scales,
+ *     FP4 A2 activations and scales emitted for an FP4 x FP4 GEMM2, top-k
+ *     contributions accumulated in FP32; Test Plan: "prequant" and "BF16"
+ *     end-to-end variants.
+ *   - "[HIP] gfx950 A8W4 fused_moe configs for DSv4.1 TP-sharded experts"
+ *     (aiter PR #6125), Motivation/Changes: MXFP4 routed experts run with
+ *     MXFP8 activations (A8W4); the top-k softmax kernel.
+ *
+ * Data formats (OCP Microscaling v1.0):
+ *   MXFP4 weights: E2M1 codes, two per byte, element 2i in the LOW nibble of
+ *   byte i; one E8M0 scale byte (value 2^(s-127)) per 32 consecutive elements
+ *   along K, row-major [rows, K/32].  MXFP8 activations: one E4M3 byte per
+ *   element with the same scales.  Scale rule: s = floor(log2 amax) - emax +
+ *   127 clamped to [0, 254] (emax 8 for E4M3, 2 for E2M1); elements rounded to
+ *   nearest even and saturated; a block whose amax is zero or fp32-subnormal
+ *   gets s = 0 and signed-zero codes.
+ *
+ * Ownership and execution:
+ *   - The caller owns every buffer (inputs, outputs, weights, workspace); all
+ *     pointers are DEVICE pointers unless stated otherwise.  The library never
+ *     allocates, frees or synchronises inside a compute call; it only enqueues
+ *     kernels on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *     default stream).
+ *   - Arguments are validated before anything is launched.  On any error the
+ *     call returns a non-zero moe_status_t, launches nothing and leaves the
+ *     outputs untouched.  A launch failure returns MOE_ERR_CUDA.
+ *   - Conditions only the device can see (a bounded wait that expired inside a
+ *     kernel) are recorded in a status word inside the workspace; read it with
+ *     moe_read_device_status after the stream has finished.
+ *   - No call throws, traps or aborts.  Kernels never __trap().
+ *   - The forward calls may be captured into a CUDA graph; a captured graph is
+ *     valid only for the pointers and sizes it was captured with.
+ *   - Supported device: compute capability 10.3 (sm_103a) only.
+ */
+#ifndef MOE_TOPK_H_
+#define MOE_TOPK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, k > E, ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,    /* H or I not a multiple of 128, E > 1024, k > 8 */
+  MOE_ERR_UNSUPPORTED_DEVICE = 3,   /* current device is not compute capability 10.3 */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace_bytes < moe_workspace_bytes(...) */
+  MOE_ERR_CUDA = 5,                 /* a CUDA runtime/driver call or a launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 6,       /* a bounded in-kernel wait expired (device status) */
+  MOE_ERR_MISALIGNED = 7            /* a pointer misses its required alignment */
+} moe_status_t;
+
+typedef enum {
+  MOE_ACT_MXFP8 = 0, /* E4M3 activation codes, one byte per element (A8W4) */
+  MOE_ACT_MXFP4 = 1  /* E2M1 activation codes, two per byte (A4W4)         */
+} moe_act_fmt_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(moe_status_t status);
+
+/*
+ * Byte offsets of the intermediates inside the forward's workspace, so that
+ * tests and tools can read the forward's own routing, permutation and
+ * quantised activations.  All offsets are 256-byte aligned.
+ *   topk_ids     int32 [T, k]      expert of slot j of token t
+ *   topk_w       fp32  [T, k]      renormalised routing weight
+ *   counts       int32 [E]         rows routed to each expert
+ *   offsets      int64 [E+1]       exclusive prefix of counts (unpadded)
+ *   padded_offsets int64 [E+1]     prefix of counts rounded up to 128 rows
+ *   mtile_base   int32 [E+1]       prefix of 128-row tiles per expert
+ *   chunk_hist   int32 [E, nchunk] per-chunk expert histogram (sort scratch)
+ *   sorted_pair  int32 [T*k]       pair q = t*k+j of the r-th row in (expert, q) order
+ *   inv          int32 [T*k]       inverse of sorted_pair: unpadded row of pair q
+ *   inv_padded   int32 [T*k]       padded row of pair q (row index into xq/a2/y2)
+ *   xq           u8 [rows_cap, H or H/2]   activation codes in padded expert order
+ *   xs           u8 [rows_cap/128][H/128][512]  their E8M0 scales, 128x4 tile layout
+ *   a2           u8 [rows_cap, I or I/2]   requantised SwiGLU output codes
+ *   a2s          u8 [rows_cap/128][I/128][512]  their scales, same tile layout
+ *   y2           fp32 [rows_cap, H]        GEMM2 output rows (unweighted)
+ *   status       uint32[8]: [0] device status bits (read them with moe_read_device_status);
+ *                [1..6] the first expired in-kernel wait, if any: [1] = 1 when recorded,
+ *                [2] barrier index, [3] phase parity, [4] CTA, [5] warp, [6] microseconds waited
+ * The 128x4 tile layout stores the scale of (row r, 32-block kb) at byte
+ *   ((r/128)*(K/128) + kb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + kb%4.
+ */
+typedef struct {
+  size_t status, topk_ids, topk_w, counts, offsets, padded_offsets, mtile_base, chunk_hist;
+  size_t sorted_pair, inv, inv_padded, xq, xs, a2, a2s, y2;
+  size_t total;      /* bytes needed == moe_workspace_bytes(...) */
+  int64_t rows_cap;  /* padded row capacity (multiple of 128) */
+  int64_t nchunk;    /* number of routing chunks (sort scratch width) */
+} moe_workspace_layout_t;
+
+/* Fill *layout for a problem size.  Returns MOE_ERR_INVALID_ARG /
+ * MOE_ERR_UNSUPPORTED_SHAPE for sizes the forward would reject. */
+moe_status_t moe_get_workspace_layout(int64_t T, int H, int I, int E, int k, moe_act_fmt_t fmt,
+                                      moe_workspace_layout_t* layout);
+
+/* Workspace bytes the forward needs for this size (0 for rejected sizes). */
+size_t moe_workspace_bytes(int64_t T, int H, int I, int E, int k, moe_act_fmt_t fmt);
+
+/*
+ * Top-k softmax gating ("[HIP] gfx950 A8W4 fused_moe configs ...", Changes:
+ * the top-k softmax kernel).  For each token t: experts ranked by fp32 logit,
+ * descending, ties to the lower expert index; topk_ids[t, j] is the j-th
+ * ranked expert; topk_w[t, j] = p_j / sum_{i<k} p_i with p the softmax of the
+ * logits (the full softmax denominator cancels).
+ *   gate_logits  fp32 [T, E] row-major, device
+ *   topk_ids     int32 [T, k] out, device;  topk_w fp32 [T, k] out, device
+ * 1 <= k <= 8, k <= E <= 1024, T >= 0 (T = 0 is a no-op).
+ */
+moe_status_t moe_topk_route(const float* gate_logits, int64_t T, int E, int k, int32_t* topk_ids,
+                            float* topk_w, void* stream);
+
+/*
+ * Stable sort of the T*k routed pairs by expert (the local form of the
+ * dispatch step of "feat(moe): FlyDSL MegaMoE fused EP-MoE integration").
+ *   topk_ids     int32 [T, k] in, device (every id in [0, E))
+ *   counts       int32 [E] out;  offsets int64 [E+1] out (offsets[E] = T*k)
+ *   sorted_pair  int32 [T*k] out: pair q = t*k+j at row r, rows ordered by
+ *                (expert ascending, q ascending)
+ *   inv          int32 [T*k] out: inv[sorted_pair[r]] = r
+ *   workspace    device scratch of at least moe_workspace_bytes(T, 128, 128, E, k,
+ *                MOE_ACT_MXFP8) bytes (only its routing-size part is used)
+ * Ids outside [0, E) are an error the device detects: they are skipped and
+ * MOE_ERR_INVALID_ARG is written to the workspace status word.
+ */
+moe_status_t moe_sort_by_expert(const int32_t* topk_ids, int64_t T, int E, int k, int32_t* counts,
+                                int64_t* offsets, int32_t* sorted_pair, int32_t* inv, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * MX quantisation of BF16 rows ("add A4W4 and FP8 P2P transport support to
+ * MegaMoE", Technical Details: per-1x32 E8M0 scales).
+ *   x_bf16   bf16 [rows, K] in, device, 16-byte aligned, K % 32 == 0
+ *   codes    u8 out: MOE_ACT_MXFP8 -> [rows, K]; MOE_ACT_MXFP4 -> [rows, K/2]
+ *   scales   u8 [rows, K/32] out, row-major E8M0
+ */
+moe_status_t moe_quantize_mx(const void* x_bf16, int64_t rows, int K, moe_act_fmt_t fmt, uint8_t* codes,
+                             uint8_t* scales, void* stream);
+
+/*
+ * The whole expert layer with MXFP8 activations and MXFP4 weights (A8W4).
+ *   x_bf16       bf16 [T, H]                       16-byte aligned
+ *   gate_logits  fp32 [T, E]
+ *   w1           MXFP4 [E, 2I, H/2]  row 2j = gate_j, row 2j+1 = up_j; 32-byte aligned
+ *   w1_scale     E8M0  [E, 2I, H/32]               4-byte aligned
+ *   w2           MXFP4 [E, H, I/2]                 32-byte aligned
+ *   w2_scale     E8M0  [E, H, I/32]                4-byte aligned
+ *   out_bf16     bf16 [T, H] out                   16-byte aligned
+ *   T >= 0 tokens (0: no-op), H and I multiples of 128, 1 <= k <= 8,
+ *   k <= E <= 1024; E is the true expert count (never inferred).
+ *   workspace    device, 256-byte aligned, >= moe_workspace_bytes(T,H,I,E,k,MOE_ACT_MXFP8)
+ * Weights are read in place (canonical layout); nothing is cached between
+ * calls, so per-layer weight pointers may change on every call.
+ */
+moe_status_t moe_a8w4_forward(const void* x_bf16, const float* gate_logits, const uint8_t* w1,
+                              const uint8_t* w1_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                              void* out_bf16, int64_t T, int H, int I, int E, int k, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * As moe_a8w4_forward with MXFP4 activations and MXFP4 A2 (A4W4: "add A4W4
+ * and FP8 P2P transport support to MegaMoE", Technical Details).  Needs
+ * moe_workspace_bytes(..., MOE_ACT_MXFP4).
+ */
+moe_status_t moe_a4w4_forward(const void* x_bf16, const float* gate_logits, const uint8_t* w1,
+                              const uint8_t* w1_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                              void* out_bf16, int64_t T, int H, int I, int E, int k, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Read the device status word a forward (or sort) left in `workspace`.
+ * Synchronises `stream`, then copies 4 bytes to the host.  *status_out gets
+ * MOE_OK or the moe_status_t a kernel recorded (MOE_ERR_DEVICE_TIMEOUT,
+ * MOE_ERR_INVALID_ARG).  Returns MOE_ERR_CUDA if the copy fails.
+ */
+moe_status_t moe_read_device_status(const void* workspace, void* stream, moe_status_t* status_out);
+
+/* Number of kernels one forward call launches for T tokens (0 for T = 0). */
+int moe_forward_launch_count(int64_t T);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_TOPK_H_ */

@@ -1,0 +1,102 @@
+"""The C-ABI library on the host: it loads without a GPU, exports every entry point the
+public header declares, and its host-side validation and workspace sizing behave as
+documented.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_moe_topk_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _declared():
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert {"moe_topk_route", "moe_a8w4_forward", "moe_a4w4_forward"} <= names
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    for code, name in moe.STATUS_NAMES.items():
+        assert moe.moe_status_string(code) == name
+    assert moe.moe_status_string(99) == "MOE_UNKNOWN_STATUS"
+
+
+def test_workspace_layout_and_bytes():
+    L = moe.moe_get_workspace_layout(8192, 7168, 3072, 384, 6)
+    R = 8192 * 6
+    assert L.rows_cap % 128 == 0 and L.rows_cap >= R and L.rows_cap <= R + 127 * 384 + 127
+    offs = [L.status, L.topk_ids, L.topk_w, L.counts, L.offsets, L.padded_offsets, L.mtile_base, L.chunk_hist,
+            L.sorted_pair, L.inv, L.inv_padded, L.xq, L.xs, L.a2, L.a2s, L.y2]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert L.y2 + 4 * 7168 * L.rows_cap <= L.total
+    assert moe.moe_workspace_bytes(8192, 7168, 3072, 384, 6) == L.total
+    a4 = moe.moe_get_workspace_layout(8192, 7168, 3072, 384, 6, moe.MOE_ACT_MXFP4)
+    assert a4.total < L.total
+    # rows_cap never exceeds R + 127 per active expert: T=1 routes to k experts
+    L1 = moe.moe_get_workspace_layout(1, 7168, 3072, 384, 6)
+    assert L1.rows_cap == 6 * 128
+    assert moe.moe_workspace_bytes(0, 7168, 3072, 384, 6) > 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((16, 250, 128, 8, 2), 2),      # H not a multiple of 128
+    ((16, 256, 96, 8, 2), 2),       # I not a multiple of 128
+    ((16, 256, 128, 8, 9), 1),      # k > E
+    ((16, 256, 128, 2048, 2), 2),   # E > 1024
+    ((16, 256, 128, 16, 9), 2),     # k > 8
+    ((-1, 256, 128, 8, 2), 1),      # negative T
+])
+def test_layout_rejects_bad_sizes(args, status):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_get_workspace_layout(*args)
+    assert ei.value.status == status
+    assert moe.moe_workspace_bytes(*args) == 0
+
+
+def test_forward_validation_before_any_launch():
+    lib = moe.lib()
+    f = lib.moe_a8w4_forward
+    ok = ctypes.c_void_p(1 << 20)  # aligned dummy addresses: validation fails before any use
+    # Only argument lists that fail host-side validation are ever passed: none of these
+    # calls reaches a CUDA API call or a launch.
+    args = [ok] * 7 + [16, 256, 128, 8, 2, ok, 1 << 30, None]
+    bad = list(args)
+    bad[0] = None
+    assert f(*bad) == 1  # null x
+    bad = list(args)
+    bad[0] = ctypes.c_void_p((1 << 20) + 8)
+    assert f(*bad) == 7  # misaligned x
+    bad = list(args)
+    bad[13] = 16
+    assert f(*bad) == 4  # workspace too small
+    bad = list(args)
+    bad[8] = 250
+    assert f(*bad) == 2  # H % 128
+    bad = list(args)
+    bad[11] = 9
+    assert f(*bad) == 1  # k > E
+
+
+def test_forward_launch_count():
+    assert moe.moe_forward_launch_count(0) == 0
+    assert moe.moe_forward_launch_count(1) == 7

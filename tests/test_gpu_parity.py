@@ -1,0 +1,279 @@
+"""GPU parity: every step of the CUDA path against the CPU oracle, through the C ABI.
+
+Bit-exact: routing ids (slot order), the permutation, the quantised activation
+codes and E8M0 scales.  Floating point: top-k weights within 1e-6 relative; the
+bf16 layer output within relative Frobenius error 5e-3 and per-row cosine
+>= 0.9999.  The A2 code mismatch rate is a diagnostic with a loose bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_moe_topk_gb300 as moe
+import oracle
+import synth
+from helpers import TOL_COS, TOL_REL, Weights, bits, compare, tile_sf_to_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.init()
+    yield
+
+
+# --------------------------------------------------------------------------- routing
+@pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (300, 64, 6, False), (4096, 384, 6, False),
+                                        (2000, 128, 3, True), (77, 1024, 8, False), (33, 5, 5, False)])
+def test_route_bit_exact(T, E, k, skew):
+    lg = synth.gate_logits(T, E, seed=T + E, skew=skew)
+    lg[0, :] = 0.25  # a fully tied row
+    if T > 3:
+        lg[3, E // 2] = lg[3, E // 3] = 50.0  # tied maxima
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    moe.moe_topk_route(lg.to(DEV), k, ids, w)
+    want_ids, want_w = oracle.route(lg.numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), want_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), want_w, rtol=1e-6, atol=0)
+
+
+# --------------------------------------------------------------------------- sort
+@pytest.mark.parametrize("T,E,k,skew", [(1, 384, 6, False), (257, 8, 2, False), (8192, 384, 6, False),
+                                        (32768, 384, 6, True), (5000, 128, 3, True)])
+def test_sort_bit_exact(T, E, k, skew):
+    lg = synth.gate_logits(T, E, seed=3, skew=skew)
+    ids_h, _ = oracle.route(lg.numpy(), k)
+    ids = torch.from_numpy(ids_h).to(DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int64, device=DEV)
+    sp = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    inv = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(T, 128, 128, E, k), dtype=torch.uint8, device=DEV)
+    moe.moe_sort_by_expert(ids, E, counts, offsets, sp, inv, ws)
+    c, o, s, i = oracle.sort(ids_h, E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(sp.cpu().numpy(), s)
+    assert np.array_equal(inv.cpu().numpy(), i)
+    assert moe.moe_read_device_status(ws) == 0
+
+
+# --------------------------------------------------------------------------- quantiser
+def _special_rows(K):
+    x = synth.x_bf16(6, K, seed=5).float()
+    x[0, :32] = 0.0
+    x[0, 32:64] = -0.0
+    x[1, :32] = 1e-39  # fp32-subnormal block
+    x[1, 32:64] = -1e-39
+    x[2, :32] = 3e38
+    x[2, 40] = -3e38
+    x[3, :] *= 1e-30
+    x[4, :] *= 1e30
+    x[5, 0:32] = torch.tensor([1.0, -1.0, 0.5, 0.25, 0.75, 1.25, 1.75, 2.5] * 4)
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("rows,K", [(6, 256), (1000, 7168), (37, 5120), (3, 2080)])
+def test_quant_bit_exact(fmt, rows, K):
+    x = synth.x_bf16(rows, K, seed=rows) if rows != 6 else _special_rows(K)
+    xd = x.to(DEV)
+    cb = K if fmt == moe.MOE_ACT_MXFP8 else K // 2
+    codes = torch.empty(rows, cb, dtype=torch.uint8, device=DEV)
+    scales = torch.empty(rows, K // 32, dtype=torch.uint8, device=DEV)
+    moe.moe_quantize_mx(xd, fmt, codes, scales)
+    want_c, want_s = oracle.quantize_rows_bf16(synth.bf16_bits(x), fmt)
+    got_c, got_s = codes.cpu().numpy(), scales.cpu().numpy()
+    assert np.array_equal(got_s, want_s)
+    bad = np.argwhere(got_c != want_c)
+    assert bad.size == 0, f"{len(bad)} code mismatches, first {bad[:5].tolist()}: " \
+                          f"got {got_c[tuple(bad[0])]:#x} want {want_c[tuple(bad[0])]:#x}"
+
+
+# --------------------------------------------------------------------------- forward
+def _run_forward(act, x, lg, W, E, k):
+    T, H = x.shape
+    I = W.I
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(T, H, I, E, k, act), dtype=torch.uint8, device=DEV)
+    f = moe.moe_a8w4_forward if act == moe.MOE_ACT_MXFP8 else moe.moe_a4w4_forward
+    f(x.to(DEV), lg.to(DEV), *W.dev, out, E, k, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    return out, ws
+
+
+def _check_intermediates(act, x, lg, W, E, k, ws, tokens=None):
+    """ids, weights, permutation and quantised activations read from the forward's own workspace."""
+    T, H = x.shape
+    I = W.I
+    v = moe.workspace_views(ws, T, H, I, E, k, act)
+    ids_h, w_h = oracle.route(lg.numpy(), k)
+    assert np.array_equal(v["topk_ids"].cpu().numpy(), ids_h)
+    np.testing.assert_allclose(v["topk_w"].cpu().numpy(), w_h, rtol=1e-6, atol=0)
+    c, o, s, i = oracle.sort(ids_h, E)
+    assert np.array_equal(v["counts"].cpu().numpy(), c)
+    assert np.array_equal(v["offsets"].cpu().numpy(), o)
+    assert np.array_equal(v["sorted_pair"].cpu().numpy(), s)
+    assert np.array_equal(v["inv"].cpu().numpy(), i)
+    poff = v["padded_offsets"].cpu().numpy()
+    inv_p = v["inv_padded"].cpu().numpy()
+    e_of_q = ids_h.reshape(-1)
+    assert np.array_equal(inv_p, poff[e_of_q] + (i - o[e_of_q]))
+    assert np.all(np.diff(poff) % 128 == 0) and np.all(np.diff(poff) >= c)
+    # quantised activations: every routed row of a (sampled) token equals the oracle's row
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    want_c, want_s = oracle.quantize_rows_bf16(synth.bf16_bits(x)[toks], act)
+    rc = int(v["layout"].rows_cap)
+    xq = v["xq"].cpu().numpy()
+    xs = tile_sf_to_rows(v["xs"].cpu().numpy(), rc, H)
+    for n, t in enumerate(toks):
+        for j in range(k):
+            r = inv_p[t * k + j]
+            assert np.array_equal(xq[r], want_c[n]), (t, j)
+            assert np.array_equal(xs[r], want_s[n]), (t, j)
+    return v, inv_p
+
+
+def _a2_mismatch(act, v, inv_p, diag, toks, k, I):
+    a2 = v["a2"].cpu().numpy()
+    rc = int(v["layout"].rows_cap)
+    a2s = tile_sf_to_rows(v["a2s"].cpu().numpy(), rc, I)
+    bad = total = 0
+    for n, t in enumerate(toks):
+        for j in range(k):
+            r = inv_p[t * k + j]
+            bad += int((a2[r] != diag["a2"][n, j]).sum()) + int((a2s[r] != diag["a2s"][n, j]).sum())
+            total += a2[r].size + a2s[r].size
+    return bad / max(total, 1)
+
+
+TINY = synth.SHAPES["tiny"]
+
+
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+def test_forward_tiny_full(act):
+    T, H, I, E, k = 16, TINY.H, TINY.I, TINY.E, TINY.k
+    W = Weights(E, H, I, seed=0, device=DEV, from_bf16=True)
+    x, lg = synth.x_bf16(T, H, 0), synth.gate_logits(T, E, 0)
+    out, ws = _run_forward(act, x, lg, W, E, k)
+    v, inv_p = _check_intermediates(act, x, lg, W, E, k, ws)
+    want, diag = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, act, diagnostics=True)
+    mis = _a2_mismatch(act, v, inv_p, diag, np.arange(T), k, I)
+    rel, cos = compare(bits(out), want)
+    assert mis < 5e-3, mis
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+@pytest.mark.parametrize("T", [1, 2, 8, 64])
+def test_forward_flash_decode(T):
+    s = synth.SHAPES["flash_decode"]
+    W = _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 0), synth.gate_logits(T, s.E, 0)
+    out, ws = _run_forward(moe.MOE_ACT_MXFP8, x, lg, W, s.E, s.k)
+    _check_intermediates(moe.MOE_ACT_MXFP8, x, lg, W, s.E, s.k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, oracle.FMT_E4M3)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+_WCACHE = {}
+
+
+def _weights(s):
+    key = (s.E, s.H, s.I)
+    if key not in _WCACHE:
+        _WCACHE.clear()
+        torch.cuda.empty_cache()
+        _WCACHE[key] = Weights(s.E, s.H, s.I, seed=0, device=DEV)
+    return _WCACHE[key]
+
+
+def _sampled_check(act, s, T, n_sample, seed=0):
+    W = _weights(s)
+    x, lg = synth.x_bf16(T, s.H, seed), synth.gate_logits(T, s.E, seed, skew=s.skew)
+    out, ws = _run_forward(act, x, lg, W, s.E, s.k)
+    rng = np.random.default_rng(T)
+    toks = np.sort(rng.choice(T, size=min(n_sample, T), replace=False))
+    # add every token of the most- and least-loaded active expert (bounded)
+    ids_h, _ = oracle.route(lg.numpy(), s.k)
+    cnt = np.bincount(ids_h.reshape(-1), minlength=s.E)
+    for e in (int(cnt.argmax()), int(np.where(cnt > 0, cnt, cnt.max() + 1).argmin())):
+        extra = np.nonzero((ids_h == e).any(1))[0][:32]
+        toks = np.union1d(toks, extra)
+    _check_intermediates(act, x, lg, W, s.E, s.k, ws, tokens=toks)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, act, tokens=toks)
+    rel, cos = compare(bits(out)[toks], want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+@pytest.mark.parametrize("T", [1, 64, 3072])
+def test_forward_draft_skewed(T):
+    _sampled_check(moe.MOE_ACT_MXFP8, synth.SHAPES["draft"], T, 48)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T,skew", [(1, False), (128, False), (8192, False), (8192, True)])
+def test_forward_pro_a8w4(T, skew):
+    s = synth.SHAPES["pro_skew" if skew else "pro"]
+    _sampled_check(moe.MOE_ACT_MXFP8, s, T, 24)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", [512])
+def test_forward_pro_a4w4(T):
+    _sampled_check(moe.MOE_ACT_MXFP4, synth.SHAPES["pro"], T, 24)
+
+
+# --------------------------------------------------------------------------- properties
+def test_forward_graph_replay_is_bit_identical():
+    s = synth.SHAPES["flash_decode"]
+    W = _weights(s)
+    T = 16
+    x, lg = synth.x_bf16(T, s.H, 1).to(DEV), synth.gate_logits(T, s.E, 1).to(DEV)
+    out_e = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+    out_g = torch.empty_like(out_e)
+    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
+    moe.moe_a8w4_forward(x, lg, *W.dev, out_e, s.E, s.k, ws)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        moe.moe_a8w4_forward(x, lg, *W.dev, out_g, s.E, s.k, ws, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_e.view(torch.int16), out_g.view(torch.int16))
+
+
+def test_forward_zero_tokens_and_zero_input():
+    s = TINY
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True)
+    out = torch.full((1, s.H), 7.0, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(0, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
+    moe.moe_a8w4_forward(torch.empty(0, s.H, dtype=torch.bfloat16, device=DEV),
+                         torch.empty(0, s.E, device=DEV), *W.dev, out[:0], s.E, s.k, ws)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+    x = torch.zeros(5, s.H, dtype=torch.bfloat16)
+    out, _ = _run_forward(moe.MOE_ACT_MXFP8, x, synth.gate_logits(5, s.E, 0), W, s.E, s.k)
+    assert torch.all(out.float() == 0.0)
+
+
+def test_forward_separated_layout_is_far_off():
+    """W1 with gate rows first and up rows second (the wrong layout) must not pass parity."""
+    s = TINY
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True)
+    T = 16
+    x, lg = synth.x_bf16(T, s.H, 0), synth.gate_logits(T, s.E, 0)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, oracle.FMT_E4M3)
+    sep = lambda a: torch.cat([a[:, 0::2], a[:, 1::2]], dim=1).contiguous()  # noqa: E731
+    W.dev = (sep(W.dev[0]), sep(W.dev[1]), W.dev[2], W.dev[3])
+    out, _ = _run_forward(moe.MOE_ACT_MXFP8, x, lg, W, s.E, s.k)
+    rel, _ = compare(bits(out), want)
+    assert rel > 0.5
