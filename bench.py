@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled MoE expert layer (A8W4, V4-Pro shape) on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--tokens T]
+
+One step = one forward of the whole layer (route, sort, quant, GEMM1+SwiGLU+A2 requant,
+GEMM2, combine) over one batch of T tokens (default 8192) of the H=7168, I=3072, E=384,
+top-6 layer with ~13.5 GB of MXFP4 weights resident in HBM.  Inputs are seeded synthetic
+data (x ~ N(0,1) bf16, logits ~ N(0,1)); weights are MXFP4 codes drawn directly (see synth).
+
+Timing: the forward is captured in a CUDA graph; W warm-up replays, then K timed replays,
+each bracketed by CUDA events on the launching stream; a 512 MiB buffer is rewritten between
+steps (outside the brackets) so L2 starts cold; barrier + synchronize on both sides; the
+time is the max over ranks.  Prints one JSON line on rank 0.
+
+Also measured in the same run: per-kernel durations (events between the kernels of the
+same launch sequence) for the roofline of the dominant kernel (GEMM1); the end-to-end
+throughput through the C ABI with pinned host buffers and the host<->device copies inside
+the timed region; a token sweep; SM clocks sampled during the timed work; and the CPU
+oracle timed on the host cores as a baseline (rank 0, N=1).
+
+--impl reference times the CPU oracle (the only reference implementation of this layer)
+on the host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer µs & routed tok/s (A8W4 7168/3072, 384x6); % HBM/MX-tensor roofline"
+SHAPE = synth.SHAPES["pro"]
+SWEEP = [1, 16, 64, 128, 512, 1024, 4096, 8192, 16384, 32768]
+FLUSH_BYTES = 512 << 20
+# canonical bytes per expert of the V4-Pro shape: W1 fp4 + W1 scales + W2 fp4 + W2 scales
+W1_BYTES = 2 * SHAPE.I * SHAPE.H // 2 + 2 * SHAPE.I * SHAPE.H // 32
+W2_BYTES = SHAPE.H * SHAPE.I // 2 + SHAPE.H * SHAPE.I // 32
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons while timed work runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", sel, "--query-gpu=" + ",".join(self.FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_workload(T, rank, device, E=SHAPE.E):
+    x = synth.x_bf16(T, SHAPE.H, seed=rank, device=device)
+    lg = synth.gate_logits(T, E, seed=rank, device=device)
+    return x, lg
+
+
+def layer_roofline(T, active, pk, E=SHAPE.E):
+    R = T * SHAPE.k
+    B = active * (W1_BYTES + W2_BYTES) + T * SHAPE.H * 2 + T * E * 4 + T * SHAPE.H * 2
+    F = 6 * R * SHAPE.H * SHAPE.I
+    mx_peak = 2.0 * pk["bf16"] * 1e12  # MXFP8 dense = 2x bf16 (nominal ratio 4.5 / 2.25 PF)
+    t_hbm, t_tc = B / (pk["hbm"] * 1e9), F / mx_peak
+    return B, F, t_hbm, t_tc
+
+
+def gemm1_algorithmic(T, active):
+    """GEMM1 bytes: active experts' W1 codes + scales, the routed activation rows and their
+    scales read, the A2 rows and scales written; flops 2 * R * 2I * H."""
+    R = T * SHAPE.k
+    B = active * W1_BYTES + R * (SHAPE.H + SHAPE.H // 32) + R * (SHAPE.I + SHAPE.I // 32)
+    F = 2 * R * 2 * SHAPE.I * SHAPE.H
+    return B, F
+
+
+def run_ours(args):
+    import block_scaled_moe_topk_gb300 as moe
+    from block_scaled_moe_topk_gb300 import build as _build
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    pk = peaks()
+    E, k, H, I = args.experts, SHAPE.k, SHAPE.H, SHAPE.I
+    T = args.tokens
+    W = synth.weights_codes(E, H, I, seed=0, device=dev)
+    sweep = sorted(set(([] if (args.no_sweep or args.quick) else SWEEP) + [T]))
+    ws = torch.empty(max(moe.moe_workspace_bytes(t, H, I, E, k) for t in sweep), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def graph_for(x, lg, out):
+        moe.moe_a8w4_forward(x, lg, *W, out, E, k, ws)  # eager warm-up (module load, tensor maps)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            moe.moe_a8w4_forward(x, lg, *W, out, E, k, ws, stream=torch.cuda.current_stream())
+        return g
+
+    def timed_replays(g, steps, warmup):
+        for _ in range(warmup):
+            flush.fill_(1)
+            g.replay()
+        barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        barrier()
+        return [a.elapsed_time(b) for a, b in evs]  # ms
+
+    def active_experts():
+        v = moe.workspace_views(ws, cur_T, H, I, E, k)
+        return int((v["counts"] > 0).sum().item())
+
+    clocks = Clocks(local)
+    # ---------------------------------------------------------------- headline
+    cur_T = T
+    x, lg = make_workload(T, rank, dev, E)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if args.quick:  # a few plain forwards (for profiler captures of a small case)
+        for _ in range(args.warmup + args.steps):
+            moe.moe_a8w4_forward(x, lg, *W, out, E, k, ws)
+        torch.cuda.synchronize()
+        clocks.stop()
+        print(json.dumps({"quick": True, "T": T, "E": E, "status": moe.moe_read_device_status(ws)}))
+        return
+    g = graph_for(x, lg, out)
+    step_ms = timed_replays(g, args.steps, args.warmup)
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = moe.moe_read_device_status(ws)
+    active = active_experts()
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # ---------------------------------------------------------------- per-kernel profile
+    prof = []
+    for i in range(max(3, min(args.steps, 20))):
+        flush.fill_(1)
+        prof.append(moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W, out, E, k, ws))
+    kern_us = {n: statistics.mean(p[n] for p in prof[1:]) for n in prof[0]}
+    g1_bytes, g1_flops = gemm1_algorithmic(T, active)
+    g1_s = kern_us["gemm1"] * 1e-6
+    t_bytes, t_flops = g1_bytes / (pk["hbm"] * 1e9), g1_flops / (2.0 * pk["bf16"] * 1e12)
+    if t_bytes >= t_flops:
+        achieved, peak, unit, bound = g1_bytes / g1_s / 1e9, pk["hbm"], "GB/s", "hbm"
+    else:
+        achieved, peak, unit, bound = g1_flops / g1_s / 1e12, 2.0 * pk["bf16"], "TFLOP/s", "tensor"
+    roofline = {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": args.traffic, "kernel": "gemm1",
+                "peak_source": pk["source"] + (" (MXFP8 = 2 x measured bf16)" if bound == "tensor" else ""),
+                "algorithmic_bytes": g1_bytes, "algorithmic_flops": g1_flops}
+
+    # ---------------------------------------------------------------- end to end, host buffers
+    x_h = x.cpu().pin_memory()
+    lg_h = lg.cpu().pin_memory()
+    out_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    x_d, lg_d = torch.empty_like(x), torch.empty_like(lg)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        moe.moe_a8w4_forward(x_d, lg_d, *W, out, E, k, ws)
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e = {"value": round(world * T * len(e2e_ms) / (e2e_total / 1e3), 1), "unit": "tok/s",
+           "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4, "d2h_bytes_per_step": out.numel() * 2,
+           "ms_per_step": round(e2e_total / len(e2e_ms), 4)}
+
+    # ---------------------------------------------------------------- token sweep
+    rows = []
+    for t_ in sweep:
+        cur_T = t_
+        xs_, lgs_ = make_workload(t_, rank, dev, E)
+        o_ = torch.empty(t_, H, dtype=torch.bfloat16, device=dev)
+        g_ = graph_for(xs_, lgs_, o_)
+        ms = statistics.median(timed_replays(g_, max(5, min(args.steps, 30)), 3))
+        act = active_experts()
+        B, F, th, tt = layer_roofline(t_, act, pk, E)
+        rows.append({"T": t_, "us": round(ms * 1e3, 2), "tok_s": round(t_ / (ms / 1e3), 1),
+                     "routed_rows_s": round(t_ * k / (ms / 1e3), 1), "active_experts": act,
+                     "bytes": B, "flops": F, "bound": "hbm" if th >= tt else "tensor",
+                     "roofline_us": round(max(th, tt) * 1e6, 2), "frac": round(max(th, tt) / (ms / 1e3), 4)})
+        del g_
+    clk = clocks.stop()
+
+    # ---------------------------------------------------------------- CPU oracle baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, lg, W, args.cpu_tokens, E)
+
+    B, F, th, tt = layer_roofline(T, active, pk, E)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 x mxfp4 -> fp32", "data": "synthetic",
+        "config": {"workload": f"V4-Pro-shaped A8W4 MoE layer H={H} I={I} E={E} top-{k}, T={T} tokens per GPU",
+                   "T": T, "H": H, "I": I, "E": E, "k": k, "weights_gb": round(E * (W1_BYTES + W2_BYTES) / 1e9, 3),
+                   "l2": "512 MiB buffer rewritten between timed steps; weights (13.5 GB) also exceed L2",
+                   "timing": "CUDA-graph replay, CUDA events per step on the launching stream",
+                   "parallelism": f"dp{world} (independent token batches, no collective)"},
+        "us_per_call": round(ms_per_step * 1e3, 2), "routed_rows_s": round(value * k, 1),
+        "layer_roofline": {"bytes": B, "flops": F, "active_experts": active, "t_hbm_us": round(th * 1e6, 2),
+                           "t_tensor_us": round(tt * 1e6, 2), "bound": "hbm" if th >= tt else "tensor",
+                           "frac": round(max(th, tt) / (ms_per_step / 1e3), 4), "peaks": pk["source"]},
+        "roofline": roofline, "kernel_us": {n: round(v, 2) for n, v in kern_us.items()},
+        "e2e": e2e, "gpu_launches": args.steps * moe.moe_forward_launch_count(T),
+        "device_status": status, "sweep": rows, "clocks": clk, "cpu_baseline": cpu,
+    }
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(x, lg, W, n_tokens, E):
+    """The oracle as it stands, on all host cores, on the first n_tokens tokens of the batch."""
+    import oracle
+    host_w = [w.cpu().numpy() for w in W]
+    xb = synth.bf16_bits(x[:n_tokens])
+    lgh = lg[:n_tokens].cpu().numpy()
+    cores = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.moe_forward(xb, lgh, *host_w, E, SHAPE.k, oracle.FMT_E4M3, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": round(n_tokens / dt, 3), "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_tokens} tokens of the same batch, whole layer per token (route, quant, GEMM1, "
+                      f"SwiGLU, A2, GEMM2, combine), fp64 accumulation; {dt:.1f} s wall"}
+
+
+def run_reference(args):
+    """CPU oracle timed on the host cores: each step is a bounded sample of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    W = synth.weights_codes(SHAPE.E, SHAPE.H, SHAPE.I, seed=0, device=dev)
+    host_w = [w.cpu().numpy() for w in W]
+    del W
+    x, lg = make_workload(args.tokens, 0, dev)
+    cores = oracle.max_threads()
+    n = args.ref_tokens
+    times = []
+    for i in range(args.warmup + args.steps):
+        sel = np.arange(i * n, (i + 1) * n) % args.tokens
+        xb = synth.bf16_bits(x[sel])
+        lgh = lg[sel].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.moe_forward(xb, lgh, *host_w, SHAPE.E, SHAPE.k, oracle.FMT_E4M3, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = n * len(times) / total
+    sample = f"{n} tokens per step of the T={args.tokens} batch, whole layer per token, fp64 accumulation"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"V4-Pro-shaped A8W4 MoE layer H={SHAPE.H} I={SHAPE.I} E={SHAPE.E} "
+                               f"top-{SHAPE.k}, T={args.tokens} tokens per GPU", "T": args.tokens},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=8192)
+    ap.add_argument("--experts", type=int, default=SHAPE.E,
+                    help="expert count (smaller values only for profiler captures of a small case)")
+    ap.add_argument("--quick", action="store_true", help="only W+K plain forwards, no report (profiling)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per GEMM1 launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -16,7 +16,8 @@ import torch
 __all__ = [
     "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_quantize_mx", "moe_a8w4_forward",
-    "moe_a4w4_forward", "moe_read_device_status", "moe_forward_launch_count", "workspace_views",
+    "moe_a4w4_forward", "moe_read_device_status", "moe_forward_launch_count", "moe_profile_forward",
+    "workspace_views",
 ]
 
 MOE_ACT_MXFP8 = 0
@@ -75,6 +76,9 @@ def lib():
     L.moe_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
     L.moe_forward_launch_count.restype = i32
     L.moe_forward_launch_count.argtypes = [i64]
+    L.moe_profile_forward.restype = i32
+    L.moe_profile_forward.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P,
+                                      ctypes.POINTER(ctypes.c_float)]
     _lib = L
     return L
 
@@ -151,6 +155,22 @@ def moe_a8w4_forward(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, work
 
 def moe_a4w4_forward(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None):
     _forward("moe_a4w4_forward", x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream)
+
+
+KERNEL_NAMES = ("route", "scan", "scatter", "quant", "gemm1", "gemm2", "combine")
+
+
+def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None):
+    """One forward with a CUDA event between kernels; returns {kernel name: microseconds}."""
+    T, H = x.shape
+    I = w2.shape[-1] * 2
+    n = moe_forward_launch_count(T)
+    us = (ctypes.c_float * max(n, 1))()
+    _check(lib().moe_profile_forward(int(fmt), _p(x), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale),
+                                     _p(out), T, H, I, int(E), int(k), _p(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream), us),
+           "moe_profile_forward")
+    return {KERNEL_NAMES[i]: float(us[i]) for i in range(n)}
 
 
 def moe_read_device_status(workspace, stream=None) -> int:

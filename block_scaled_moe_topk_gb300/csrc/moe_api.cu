@@ -118,10 +118,15 @@ uint64_t wait_timeout_ns() {
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
+// The forward's launch sequence.  With `ev` (kForwardKernels + 1 events) an event is
+// recorded before the first kernel and after every kernel, for per-kernel timing.
+constexpr int kForwardKernels = 7;  // route, scan, scatter, quant, gemm1, gemm2, combine
+
 moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2,
                      const uint8_t* w2s, void* out, int64_t T, int H, int I, int E, int k, void* ws,
-                     size_t ws_bytes, void* stream, moe_act_fmt_t fmt) {
-  if (!x || !logits || !w1 || !w1s || !w2 || !w2s || !out || !ws) return MOE_ERR_INVALID_ARG;
+                     size_t ws_bytes, void* stream, moe_act_fmt_t fmt, cudaEvent_t* ev = nullptr) {
+  // with T == 0 nothing is read or written, so empty x / logits / out may be null
+  if ((T > 0 && (!x || !logits || !out)) || !w1 || !w1s || !w2 || !w2s || !ws) return MOE_ERR_INVALID_ARG;
   moe_workspace_layout_t L;
   moe_status_t st = layout(T, H, I, E, k, fmt, &L);
   if (st != MOE_OK) return st;
@@ -147,15 +152,23 @@ moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, cons
   int32_t* chunk_hist = reinterpret_cast<int32_t*>(at(L.chunk_hist));
   int32_t* inv_padded = reinterpret_cast<int32_t*>(at(L.inv_padded));
 
+  int evi = 0;
+  auto mark = [&]() { return ev ? cudaEventRecord(ev[evi++], s) : cudaSuccess; };
+  MOE_CUDA_TRY(mark());
   moe::RouteArgs ra{logits, T, E, k, ids, tw, chunk_hist, L.nchunk, status, 1};
   MOE_CUDA_TRY(moe::launch_route(ra, s));
+  MOE_CUDA_TRY(mark());
   moe::SortArgs sa{ids, T, E, k, chunk_hist, L.nchunk, counts, offsets, poff, mtb,
                    reinterpret_cast<int32_t*>(at(L.sorted_pair)), reinterpret_cast<int32_t*>(at(L.inv)),
                    inv_padded, status};
-  MOE_CUDA_TRY(moe::launch_sort(sa, s));
+  MOE_CUDA_TRY(moe::launch_scan(sa, s));
+  MOE_CUDA_TRY(mark());
+  MOE_CUDA_TRY(moe::launch_scatter(sa, s));
+  MOE_CUDA_TRY(mark());
   const int afmt = fmt == MOE_ACT_MXFP8 ? 0 : 1;
   moe::QuantArgs qa{static_cast<const uint16_t*>(x), T, H, afmt, at(L.xq), at(L.xs), inv_padded, k};
   MOE_CUDA_TRY(moe::launch_quant(qa, s));
+  MOE_CUDA_TRY(mark());
 
   const int64_t mtiles_cap = L.rows_cap / kRowTile;
   moe::GemmArgs g1{};
@@ -179,8 +192,8 @@ moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, cons
   g1.timeout_ns = wait_timeout_ns();
   g1.num_sms = dev.num_sms;
   cudaError_t err = moe::launch_gemm(g1, s);
-  if (err == cudaErrorInvalidValue || err == cudaErrorNotSupported) return MOE_ERR_CUDA;
   MOE_CUDA_TRY(err);
+  MOE_CUDA_TRY(mark());
 
   moe::GemmArgs g2 = g1;
   g2.epilogue = 1;
@@ -195,9 +208,11 @@ moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, cons
   g2.out_sf = nullptr;
   g2.out_f32 = reinterpret_cast<float*>(at(L.y2));
   MOE_CUDA_TRY(moe::launch_gemm(g2, s));
+  MOE_CUDA_TRY(mark());
 
   moe::CombineArgs ca{reinterpret_cast<const float*>(at(L.y2)), tw, inv_padded, T, H, k, static_cast<uint16_t*>(out)};
   MOE_CUDA_TRY(moe::launch_combine(ca, s));
+  MOE_CUDA_TRY(mark());
   return MOE_OK;
 }
 
@@ -313,6 +328,32 @@ moe_status_t moe_read_device_status(const void* ws, void* stream, moe_status_t* 
   return MOE_OK;
 }
 
-int moe_forward_launch_count(int64_t T) { return T > 0 ? 7 : 0; }
+int moe_forward_launch_count(int64_t T) { return T > 0 ? kForwardKernels : 0; }
+
+moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* logits, const uint8_t* w1,
+                                 const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T,
+                                 int H, int I, int E, int k, void* ws, size_t ws_bytes, void* stream,
+                                 float* kernel_us) {
+  if (!kernel_us) return MOE_ERR_INVALID_ARG;
+  if (fmt != MOE_ACT_MXFP8 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[kForwardKernels + 1] = {};
+  moe_status_t st = MOE_OK;
+  for (int i = 0; i <= kForwardKernels && st == MOE_OK; ++i)
+    if (cudaEventCreate(&ev[i]) != cudaSuccess) st = MOE_ERR_CUDA;
+  if (st == MOE_OK) st = forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt, ev);
+  if (st == MOE_OK && T > 0) {
+    if (cudaEventSynchronize(ev[kForwardKernels]) != cudaSuccess) st = MOE_ERR_CUDA;
+    for (int i = 0; i < kForwardKernels && st == MOE_OK; ++i) {
+      float ms = 0.0f;
+      if (cudaEventElapsedTime(&ms, ev[i], ev[i + 1]) != cudaSuccess) st = MOE_ERR_CUDA;
+      kernel_us[i] = ms * 1000.0f;
+    }
+  } else if (st == MOE_OK) {
+    for (int i = 0; i < kForwardKernels; ++i) kernel_us[i] = 0.0f;
+  }
+  for (int i = 0; i <= kForwardKernels; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  return st;
+}
 
 }  // extern "C"

@@ -52,7 +52,9 @@ struct SortArgs {
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 // Histogram of externally supplied ids (standalone sort entry point).
 cudaError_t launch_histogram(const SortArgs& a, cudaStream_t s);
-// sort.cu: per-expert chunk bases + offsets, then the stable scatter.
+// sort.cu: per-expert chunk bases + offsets (scan), then the stable scatter.
+cudaError_t launch_scan(const SortArgs& a, cudaStream_t s);
+cudaError_t launch_scatter(const SortArgs& a, cudaStream_t s);
 cudaError_t launch_sort(const SortArgs& a, cudaStream_t s);
 
 // quant.cu

@@ -125,13 +125,21 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
 
 }  // namespace
 
-cudaError_t launch_sort(const SortArgs& a, cudaStream_t s) {
+cudaError_t launch_scan(const SortArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
   scan_kernel<<<1, kScanThreads, 0, s>>>(a);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const SortArgs& a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
   scatter_kernel<<<(unsigned)a.nchunk, 32, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_sort(const SortArgs& a, cudaStream_t s) {
+  const cudaError_t err = launch_scan(a, s);
+  return err != cudaSuccess ? err : launch_scatter(a, s);
 }
 
 }  // namespace moe

@@ -174,7 +174,8 @@ moe_status_t moe_quantize_mx(const void* x_bf16, int64_t rows, int K, moe_act_fm
  *   w2           MXFP4 [E, H, I/2]                 32-byte aligned
  *   w2_scale     E8M0  [E, H, I/32]                4-byte aligned
  *   out_bf16     bf16 [T, H] out                   16-byte aligned
- *   T >= 0 tokens (0: no-op), H and I multiples of 128, 1 <= k <= 8,
+ *   T >= 0 tokens (0: no-op; x, logits and out may then be NULL), H and I
+ *   multiples of 128, 1 <= k <= 8,
  *   k <= E <= 1024; E is the true expert count (never inferred).
  *   workspace    device, 256-byte aligned, >= moe_workspace_bytes(T,H,I,E,k,MOE_ACT_MXFP8)
  * Weights are read in place (canonical layout); nothing is cached between
@@ -205,6 +206,22 @@ moe_status_t moe_read_device_status(const void* workspace, void* stream, moe_sta
 
 /* Number of kernels one forward call launches for T tokens (0 for T = 0). */
 int moe_forward_launch_count(int64_t T);
+
+/*
+ * Profiling form of the forward: enqueues exactly the launch sequence of
+ * moe_a8w4_forward (fmt = MOE_ACT_MXFP8) or moe_a4w4_forward (MOE_ACT_MXFP4)
+ * with a CUDA event recorded before the first kernel and after each kernel,
+ * waits for the last event, and writes the duration of each kernel in
+ * microseconds to kernel_us[moe_forward_launch_count(T)] (HOST array), in
+ * launch order: route, scan, scatter, quant, gemm1, gemm2, combine.
+ * Arguments and errors as for the forward; additionally synchronises on its
+ * own events (so it is not graph-capturable) and creates/destroys them.
+ */
+moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x_bf16, const float* gate_logits,
+                                 const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
+                                 const uint8_t* w2_scale, void* out_bf16, int64_t T, int H, int I, int E,
+                                 int k, void* workspace, size_t workspace_bytes, void* stream,
+                                 float* kernel_us);
 
 #ifdef __cplusplus
 }

@@ -277,3 +277,18 @@ def test_forward_separated_layout_is_far_off():
     out, _ = _run_forward(moe.MOE_ACT_MXFP8, x, lg, W, s.E, s.k)
     rel, _ = compare(bits(out), want)
     assert rel > 0.5
+
+
+def test_profile_forward_matches_forward():
+    s = TINY
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True)
+    T = 16
+    x, lg = synth.x_bf16(T, s.H, 0).to(DEV), synth.gate_logits(T, s.E, 0).to(DEV)
+    out_a = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+    out_b = torch.empty_like(out_a)
+    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
+    moe.moe_a8w4_forward(x, lg, *W.dev, out_a, s.E, s.k, ws)
+    us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws)
+    torch.cuda.synchronize()
+    assert list(us) == list(moe.KERNEL_NAMES) and all(v > 0 for v in us.values())
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
