@@ -15,7 +15,8 @@ import torch
 
 __all__ = [
     "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "lib", "moe_status_string", "moe_workspace_bytes",
-    "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_quantize_mx", "moe_a8w4_forward",
+    "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
+    "moe_quantize_mx", "moe_a8w4_forward",
     "moe_a4w4_forward", "moe_read_device_status", "moe_forward_launch_count", "moe_profile_forward",
     "workspace_views",
 ]
@@ -131,6 +132,18 @@ def moe_sort_by_expert(topk_ids, E, counts, offsets, sorted_pair, inv, workspace
     _check(lib().moe_sort_by_expert(_p(topk_ids), T, int(E), k, _p(counts), _p(offsets), _p(sorted_pair), _p(inv),
                                     _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_sort_by_expert")
+
+
+def moe_sort_by_expert_noalloc(topk_ids, E, counts, offsets, sorted_pair, inv, stream=None):
+    """moe_sort_by_expert for callers that cannot provide scratch memory: the library uses
+    its own fixed 4 MiB device array instead of a workspace (see include/moe_topk.h)."""
+    f = lib().moe_sort_by_expert_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    T, k = topk_ids.shape
+    _check(f(_p(topk_ids), T, int(E), k, _p(counts), _p(offsets), _p(sorted_pair), _p(inv), _stream(stream)),
+           "moe_sort_by_expert_noalloc")
 
 
 def moe_quantize_mx(x, fmt, codes, scales, stream=None):

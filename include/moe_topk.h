@@ -156,6 +156,29 @@ moe_status_t moe_sort_by_expert(const int32_t* topk_ids, int64_t T, int E, int k
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * moe_sort_by_expert without a workspace argument.  The pages have no counterpart to
+ * this entry point; it exists for callers that cannot give the library scratch memory:
+ * runtimes that plan every device buffer ahead of time and hand a kernel only its
+ * inputs and outputs (fixed arenas in embedded or real-time deployments, plugin
+ * interfaces of other frameworks that expose no allocator), and latency-critical hosts
+ * that must not call cudaMalloc, which can synchronise the whole device.
+ *   Same arguments, results and errors as moe_sort_by_expert, minus the workspace.
+ *   Scratch: a fixed 4 MiB array inside the library, present on every GPU that loads
+ *   it until the process exits.  It must hold 256 + 4 * E * ceil(T / 256) bytes;
+ *   larger T * E is rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything runs
+ *   (with E = 384 that allows T up to 698,880 tokens).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any
+ *   stream capture.  The call allocates nothing.
+ *   Every call on a device shares the array: two calls whose kernels overlap on the
+ *   GPU (different streams, or several host threads) race on it and must be
+ *   serialised by the caller.  Ids outside [0, E) are skipped as in
+ *   moe_sort_by_expert, but the flag they raise stays inside the library.
+ */
+moe_status_t moe_sort_by_expert_noalloc(const int32_t* topk_ids, int64_t T, int E, int k, int32_t* counts,
+                                        int64_t* offsets, int32_t* sorted_pair, int32_t* inv, void* stream);
+
+/*
  * MX quantisation of BF16 rows ("add A4W4 and FP8 P2P transport support to
  * MegaMoE", Technical Details: per-1x32 E8M0 scales).
  *   x_bf16   bf16 [rows, K] in, device, 16-byte aligned, K % 32 == 0
