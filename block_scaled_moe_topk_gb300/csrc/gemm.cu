@@ -15,10 +15,15 @@
 //   warp 1      TMEM owner and MMA issuer (one thread): tcgen05.cp of the scales to TMEM, then
 //               tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1, scale_vec 1X) or kind::mxf4 (E2M1 x E2M1,
 //               scale_vec 2X) into a 128x256 fp32 accumulator in TMEM;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one routed row) per
-//               thread.
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one routed row) per
+//               thread; warps 2-5 take columns [0, 128), warps 6-9 columns [128, 256).  Each
+//               thread pulls its 128 columns into registers, releases TMEM at once, and only
+//               then runs the SwiGLU / requant / store work, so that work overlaps the next
+//               tile's MMAs.
 // A 4-deep shared-memory ring with full/empty mbarriers overlaps the weight stream with the
-// MMAs.  Every wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
+// MMAs; weight tiles are also prefetched into L2 kPrefetch stages ahead (bulk tensor
+// prefetch) and each tile's canonical weight-scale block is prefetched at the tile start, so
+// L2 serves as extra pipeline depth beyond what shared memory holds.  Every wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
 // status word, lets its own copies and MMAs drain (again bounded), frees TMEM and returns.
 #include <cuda.h>
 
@@ -32,7 +37,9 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;    // producer, MMA, 8 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr int kPrefetch = 8;     // weight tiles warmed in L2 this many stages ahead
 constexpr int kABytes = kRowTile * 128;   // 128 rows x 128 bytes
 constexpr int kBBytes = kNTile * 128;     // 256 rows x 128 bytes (shared-memory footprint)
 constexpr int kSfaOff = kABytes + kBBytes;
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       mbar_init(empty_bar(s), 1);      // tcgen05.commit
     }
     mbar_init(tmem_full_bar, 1);
-    mbar_init(tmem_empty_bar, 4);      // one arrival per epilogue warp
+    mbar_init(tmem_empty_bar, kEpiWarps);  // one arrival per epilogue warp
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -210,6 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const int64_t row0 = p.padded_offsets[tc.e] + (int64_t)tc.mt * kRowTile;
       const int n0 = tc.nt * kNTile;
       const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
+      if (lane == 0) {
+        // this tile's first weight stages and its whole (contiguous) weight-scale block
+        for (int ks = 0; ks < kPrefetch && ks < nks; ++ks) tma_prefetch_3d(&p.tmap_w, ks * 128, n0, tc.e);
+        const uint32_t sf_bytes = (uint32_t)kNTile * (uint32_t)(K / 32);
+        if ((reinterpret_cast<uintptr_t>(wsf_rows) & 15) == 0 && (sf_bytes & 15) == 0)
+          bulk_prefetch_l2(wsf_rows, sf_bytes);
+      }
       for (int ks = 0; ks < nks; ++ks) {
         if (!warp_wait(empty_bar(slot), phase ^ 1u, sync, p.timeout_ns)) {
           ok = false;
@@ -221,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(kABytes + TR::kBTxBytes + katoms * 512));
           tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
           tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
+          if (ks + kPrefetch < nks) tma_prefetch_3d(&p.tmap_w, (ks + kPrefetch) * 128, n0, tc.e);
           bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
                     (uint32_t)katoms * 512u, full_bar(slot));
         }
@@ -310,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may read
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;  // accumulator columns [half*128, half*128 + 128)
     uint32_t acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile tc = decode_tile(tile, p.mtile_base, p.E, NT);
@@ -319,24 +335,28 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const int64_t prow = p.padded_offsets[tc.e] + row_local;
       if (!warp_wait(tmem_full_bar, acc_phase, sync, p.timeout_ns)) break;
       tc_fence_after();
-      const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16);
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
+      float acc[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(taddr + c * 32, acc + 32 * c);
+      tc_wait_ld();
+      // the accumulator is in registers: hand TMEM back to the MMA warp before the math
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty_bar);
+      acc_phase ^= 1u;
       if (EPI == 0) {
         const int I = p.N / 2;
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          float acc[64];
-          tc_ld_32x32b_x32(trow + blk * 64, acc);
-          tc_ld_32x32b_x32(trow + blk * 64 + 32, acc + 32);
-          tc_wait_ld();
-          float h[32];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = silu_mul(acc[2 * i], acc[2 * i + 1]);  // h in place
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const float* h = acc + 32 * blk;
           float amax = 0.0f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            h[i] = silu_mul(acc[2 * i], acc[2 * i + 1]);
-            amax = fmaxf(amax, fabsf(h[i]));
-          }
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
           const MxScale sc = mx_scale<ACT>(amax);
-          const int kb = tc.nt * 4 + blk;  // 32-wide block of h
+          const int kb = tc.nt * 4 + half * 2 + blk;  // 32-wide block of h
           if (valid) {
             if (ACT == 0) {
               uint4* dst = reinterpret_cast<uint4*>(p.out_codes + prow * I + kb * 32);
@@ -352,24 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             p.out_sf[sf_tile_offset(prow, kb, I)] = sc.byte;
           }
         }
-      } else {
-        float* dst_row = p.out_f32 + prow * p.N + tc.nt * kNTile;
-#pragma unroll 1
-        for (int c = 0; c < kNTile / 32; ++c) {
-          float v[32];
-          tc_ld_32x32b_x32(trow + c * 32, v);
-          tc_wait_ld();
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst_row + c * 32);
+      } else if (valid) {
+        float4* d4 = reinterpret_cast<float4*>(p.out_f32 + prow * p.N + tc.nt * kNTile + half * 128);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          }
-        }
+        for (int i = 0; i < 32; ++i) d4[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty_bar);
-      acc_phase ^= 1u;
     }
   }
 

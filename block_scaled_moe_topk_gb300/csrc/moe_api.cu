@@ -8,7 +8,7 @@
 #include <mutex>
 
 #include "moe_internal.h"
-#include "../../include/moe_topk.h"
+#include "moe_topk.h"
 
 namespace {
 

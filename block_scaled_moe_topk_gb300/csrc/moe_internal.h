@@ -10,7 +10,7 @@ namespace moe {
 
 // Routing chunk: tokens handled by one routing block (its expert histogram is one
 // column of chunk_hist).
-constexpr int kTokensPerChunk = 256;
+constexpr int kTokensPerChunk = 32;  // 8 warps x 4 tokens: enough warps to route T=8192 on 152 SMs
 constexpr int kRowTile = 128;   // rows per GEMM M tile; expert segments are padded to it
 constexpr int kNTile = 256;     // output columns per GEMM N tile
 constexpr int kMaxExperts = 1024;

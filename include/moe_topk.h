@@ -164,9 +164,9 @@ moe_status_t moe_sort_by_expert(const int32_t* topk_ids, int64_t T, int E, int k
  * that must not call cudaMalloc, which can synchronise the whole device.
  *   Same arguments, results and errors as moe_sort_by_expert, minus the workspace.
  *   Scratch: a fixed 4 MiB array inside the library, present on every GPU that loads
- *   it until the process exits.  It must hold 256 + 4 * E * ceil(T / 256) bytes;
+ *   it until the process exits.  It must hold 256 + 4 * E * ceil(T / 32) bytes;
  *   larger T * E is rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything runs
- *   (with E = 384 that allows T up to 698,880 tokens).
+ *   (with E = 384 that allows T up to 87,360 tokens).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before any
  *   stream capture.  The call allocates nothing.

@@ -52,7 +52,7 @@ def test_noalloc_sort_matches_workspace_sort_on_two_calls_in_a_row():
 
 
 def test_noalloc_sort_rejects_sizes_beyond_its_scratch():
-    T, E, k = 300000, 1024, 1  # 4 * 1024 * ceil(300000 / 256) bytes > 4 MiB
+    T, E, k = 300000, 1024, 1  # 4 * 1024 * ceil(300000 / 32) bytes > 4 MiB
     ids = torch.zeros(T, k, dtype=torch.int32, device=DEV)
     out = _outputs(T, E, k)
     with pytest.raises(moe.MoeError) as ei:
