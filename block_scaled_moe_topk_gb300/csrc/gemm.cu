@@ -21,9 +21,9 @@
 //               then runs the SwiGLU / requant / store work, so that work overlaps the next
 //               tile's MMAs.
 // A 4-deep shared-memory ring with full/empty mbarriers overlaps the weight stream with the
-// MMAs; weight tiles are also prefetched into L2 kPrefetch stages ahead (bulk tensor
-// prefetch) and each tile's canonical weight-scale block is prefetched at the tile start, so
-// L2 serves as extra pipeline depth beyond what shared memory holds.  Every wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
+// MMAs; each tile's canonical weight-scale block is prefetched into L2 at the tile start.
+// The producer loop is short on purpose (its per-stage issue cost, not DRAM latency, set the
+// pace of an earlier version): barrier probes are inlined, addressing is hoisted per tile.  Every wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
 // status word, lets its own copies and MMAs drain (again bounded), frees TMEM and returns.
 #include <cuda.h>
 
@@ -39,7 +39,6 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kThreads = 320;    // producer, MMA, 8 epilogue warps
 constexpr int kEpiWarps = 8;
-constexpr int kPrefetch = 8;     // weight tiles warmed in L2 this many stages ahead
 constexpr int kABytes = kRowTile * 128;   // 128 rows x 128 bytes
 constexpr int kBBytes = kNTile * 128;     // 256 rows x 128 bytes (shared-memory footprint)
 constexpr int kSfaOff = kABytes + kBBytes;
@@ -151,8 +150,12 @@ __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const S
 // Warp-uniform form: every lane polls, and the warp proceeds only if all lanes saw the
 // phase complete, so no lane can run ahead into a .sync.aligned tcgen05 instruction
 // while another one is leaving on the abort path.
+// The common case (the phase already completed) costs one probe and one vote; the timed
+// polling loop only runs after a miss.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns) {
-  const bool ok = bounded_wait(bar, parity, s, limit_ns);
+  bool ok = mbar_try_wait(bar, parity);
+  if (__all_sync(0xffffffffu, ok)) return true;
+  if (!ok) ok = bounded_wait(bar, parity, s, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -217,9 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const int64_t row0 = p.padded_offsets[tc.e] + (int64_t)tc.mt * kRowTile;
       const int n0 = tc.nt * kNTile;
       const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
+      const int64_t sf_row32 = (int64_t)32 * (K / 32);        // 32 weight rows of scales
+      const uint8_t* lane_sf = wsf_rows + (int64_t)lane * (K / 32);
       if (lane == 0) {
-        // this tile's first weight stages and its whole (contiguous) weight-scale block
-        for (int ks = 0; ks < kPrefetch && ks < nks; ++ks) tma_prefetch_3d(&p.tmap_w, ks * 128, n0, tc.e);
+        // warm L2 with this tile's whole (contiguous) weight-scale block
         const uint32_t sf_bytes = (uint32_t)kNTile * (uint32_t)(K / 32);
         if ((reinterpret_cast<uintptr_t>(wsf_rows) & 15) == 0 && (sf_bytes & 15) == 0)
           bulk_prefetch_l2(wsf_rows, sf_bytes);
@@ -235,15 +239,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(kABytes + TR::kBTxBytes + katoms * 512));
           tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
           tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
-          if (ks + kPrefetch < nks) tma_prefetch_3d(&p.tmap_w, (ks + kPrefetch) * 128, n0, tc.e);
           bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
                     (uint32_t)katoms * 512u, full_bar(slot));
         }
-        for (int item = lane; item < kNTile * katoms; item += 32) {
-          const int r = item & (kNTile - 1), ka = item / kNTile;
-          const uint8_t* src = wsf_rows + (int64_t)r * (K / 32) + ks * (TR::kKPerStage / 32) + ka * 4;
-          const uint32_t dst = st + kSfbOff + ka * 1024 + (r >> 7) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
-          cp_async_4(dst, src);
+        // weight scales: this lane copies rows lane + 32*jj (jj < 8) of each k-atom, 4 bytes each,
+        // into the 128x4 tile layout (row r -> byte (r%32)*16 + ((r%128)/32)*4 of tile r/128)
+        {
+          const uint8_t* src_k = lane_sf + ks * (TR::kKPerStage / 32);
+          const uint32_t dst_k = st + kSfbOff + (uint32_t)lane * 16u;
+#pragma unroll
+          for (int j = 0; j < 8 * kAtomsPerStage; ++j) {
+            const int jj = j & 7, ka = j >> 3;
+            if (ka < katoms)
+              cp_async_4(dst_k + ka * 1024 + (jj >> 2) * 512 + (jj & 3) * 4, src_k + jj * sf_row32 + ka * 4);
+          }
         }
         cp_async_arrive_noinc(full_bar(slot));
         armed_parity[slot] = (int)phase;
