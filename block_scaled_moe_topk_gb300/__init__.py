@@ -17,7 +17,8 @@ __all__ = [
     "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
     "moe_quantize_mx", "moe_a8w4_forward",
-    "moe_a4w4_forward", "moe_read_device_status", "moe_forward_launch_count", "moe_profile_forward",
+    "moe_a4w4_forward", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
+    "moe_read_device_status", "moe_forward_launch_count", "moe_profile_forward",
     "workspace_views",
 ]
 
@@ -69,7 +70,8 @@ def lib():
     L.moe_sort_by_expert.argtypes = [P, i64, i32, i32, P, P, P, P, P, sz, P]
     L.moe_quantize_mx.restype = i32
     L.moe_quantize_mx.argtypes = [P, i64, i32, i32, P, P, P]
-    for name in ("moe_a8w4_forward", "moe_a4w4_forward"):
+    for name in ("moe_a8w4_forward", "moe_a4w4_forward", "moe_a8w4_forward_prepacked",
+                 "moe_a4w4_forward_prepacked"):
         f = getattr(L, name)
         f.restype = i32
         f.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P]
@@ -78,8 +80,10 @@ def lib():
     L.moe_forward_launch_count.restype = i32
     L.moe_forward_launch_count.argtypes = [i64]
     L.moe_profile_forward.restype = i32
-    L.moe_profile_forward.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P,
+    L.moe_profile_forward.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P, i32,
                                       ctypes.POINTER(ctypes.c_float)]
+    L.moe_prepack_scales.restype = i32
+    L.moe_prepack_scales.argtypes = [P, i64, i32, P, P]
     _lib = L
     return L
 
@@ -170,10 +174,31 @@ def moe_a4w4_forward(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, work
     _forward("moe_a4w4_forward", x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream)
 
 
+def moe_prepack_scales(scales, tiled, stream=None):
+    """E8M0 scales [..., rows, K/32] (any leading dims) -> 128x4 tile layout into ``tiled`` (same bytes)."""
+    K = scales.shape[-1] * 32
+    rows = scales.numel() // (K // 32)
+    _check(lib().moe_prepack_scales(_p(scales), rows, K, _p(tiled), _stream(stream)), "moe_prepack_scales")
+
+
+def moe_a8w4_forward_prepacked(x, gate_logits, w1, w1_scale_tiled, w2, w2_scale_tiled, out, E, k, workspace,
+                               stream=None):
+    """moe_a8w4_forward with both weight-scale tensors prepacked by moe_prepack_scales."""
+    _forward("moe_a8w4_forward_prepacked", x, gate_logits, w1, w1_scale_tiled, w2, w2_scale_tiled, out, E, k,
+             workspace, stream)
+
+
+def moe_a4w4_forward_prepacked(x, gate_logits, w1, w1_scale_tiled, w2, w2_scale_tiled, out, E, k, workspace,
+                               stream=None):
+    _forward("moe_a4w4_forward_prepacked", x, gate_logits, w1, w1_scale_tiled, w2, w2_scale_tiled, out, E, k,
+             workspace, stream)
+
+
 KERNEL_NAMES = ("route", "scan", "scatter", "quant", "gemm1", "gemm2", "combine")
 
 
-def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None):
+def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None,
+                        prepacked_scales=False):
     """One forward with a CUDA event between kernels; returns {kernel name: microseconds}."""
     T, H = x.shape
     I = w2.shape[-1] * 2
@@ -181,7 +206,8 @@ def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E,
     us = (ctypes.c_float * max(n, 1))()
     _check(lib().moe_profile_forward(int(fmt), _p(x), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale),
                                      _p(out), T, H, I, int(E), int(k), _p(workspace),
-                                     workspace.numel() * workspace.element_size(), _stream(stream), us),
+                                     workspace.numel() * workspace.element_size(), _stream(stream),
+                                     int(bool(prepacked_scales)), us),
            "moe_profile_forward")
     return {KERNEL_NAMES[i]: float(us[i]) for i in range(n)}
 

@@ -9,9 +9,10 @@
 //   GEMM2 (EPI=1): y2[r, n] = sum_I a2[r, I] * W2[e, n, I], stored as fp32 rows.
 //
 // Tiles are 128 routed rows (one expert's padded segment) x 256 output columns.  Per CTA:
-//   warp 0      producer: TMA (activation tile 128x128B, weight tile 256x128B), a bulk copy of
-//               the activation scales (already in the 128x4 tile layout) and 4-byte cp.async
-//               copies that rearrange the canonical weight scales into that layout;
+//   warp 0      producer: TMA (activation tile 128x128B, weight tile 256x128B) and a bulk copy
+//               of the activation scales (already in the 128x4 tile layout);
+//   warp 10     producer: 4-byte cp.async copies that rearrange the canonical weight scales
+//               into that layout, in parallel with warp 0;
 //   warp 1      TMEM owner and MMA issuer (one thread): tcgen05.cp of the scales to TMEM, then
 //               tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1, scale_vec 1X) or kind::mxf4 (E2M1 x E2M1,
 //               scale_vec 2X) into a 128x256 fp32 accumulator in TMEM;
@@ -37,8 +38,9 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 320;    // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 352;    // TMA producer, MMA, 8 epilogue warps, weight-scale copier
 constexpr int kEpiWarps = 8;
+constexpr int kScaleWarp = 10;
 constexpr int kABytes = kRowTile * 128;   // 128 rows x 128 bytes
 constexpr int kBBytes = kNTile * 128;     // 256 rows x 128 bytes (shared-memory footprint)
 constexpr int kSfaOff = kABytes + kBBytes;
@@ -54,7 +56,7 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_act;
   CUtensorMap tmap_w;
   const uint8_t* act_sf;
-  const uint8_t* w_sf;
+  const uint8_t* w_sf;    // canonical [E, N, K/32], or the 128x4 tile layout when w_sf_tiled
   const int32_t* counts;
   const int64_t* padded_offsets;
   const int32_t* mtile_base;
@@ -64,6 +66,7 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   uint32_t* status;
   uint64_t timeout_ns;
   int E, N, K;
+  int w_sf_tiled;
 };
 
 template <int ACT>
@@ -183,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1 + 32);  // producer's expect_tx arrive + 32 cp.async arrivals
+      // TMA warp's expect_tx arrive (+ 32 cp.async arrivals of the scale warp for canonical scales)
+      mbar_init(full_bar(s), p.w_sf_tiled ? 1 : 1 + 32);
       mbar_init(empty_bar(s), 1);      // tcgen05.commit
     }
     mbar_init(tmem_full_bar, 1);
@@ -207,8 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const int nks = (K + TR::kKPerStage - 1) / TR::kKPerStage;
   const int64_t total_tiles = (int64_t)p.mtile_base[p.E] * NT;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+  if (warp == 0 || (warp == kScaleWarp && !p.w_sf_tiled)) {
+    // ------------------------------------------------------------------ producers
+    // Warp 0 issues the TMA loads of a stage; warp 10 gathers the stage's weight scales
+    // with 4-byte cp.async copies.  Both walk the same stages and wait for the same free
+    // slots, so the two kinds of copy are issued in parallel.
+    const bool tma_warp = warp == 0;
     int slot = 0;
     uint32_t phase = 0;
     int armed_parity[kStages];
@@ -222,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
       const int64_t sf_row32 = (int64_t)32 * (K / 32);        // 32 weight rows of scales
       const uint8_t* lane_sf = wsf_rows + (int64_t)lane * (K / 32);
-      if (lane == 0) {
+      if (!tma_warp && !p.w_sf_tiled && lane == 0) {
         // warm L2 with this tile's whole (contiguous) weight-scale block
         const uint32_t sf_bytes = (uint32_t)kNTile * (uint32_t)(K / 32);
         if ((reinterpret_cast<uintptr_t>(wsf_rows) & 15) == 0 && (sf_bytes & 15) == 0)
@@ -235,26 +243,36 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         }
         const int katoms = min(TR::kKPerStage, K - ks * TR::kKPerStage) / 128;
         const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(kABytes + TR::kBTxBytes + katoms * 512));
+        if (tma_warp && lane == 0) {
+          mbar_arrive_expect_tx(full_bar(slot),
+                                (uint32_t)(kABytes + TR::kBTxBytes + katoms * 512 + (p.w_sf_tiled ? 2 * katoms * 512 : 0)));
           tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
           tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
           bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
                     (uint32_t)katoms * 512u, full_bar(slot));
+          if (p.w_sf_tiled) {
+            // prepacked weight scales: one contiguous run of k-atoms per 128-row half of the tile
+#pragma unroll
+            for (int na = 0; na < 2; ++na)
+              bulk_load(st + kSfbOff + na * (kAtomsPerStage * 512),
+                        p.w_sf + ((((int64_t)tc.e * p.N + n0) / 128 + na) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
+                        (uint32_t)katoms * 512u, full_bar(slot));
+          }
         }
         // weight scales: this lane copies rows lane + 32*jj (jj < 8) of each k-atom, 4 bytes each,
         // into the 128x4 tile layout (row r -> byte (r%32)*16 + ((r%128)/32)*4 of tile r/128)
-        {
+        if (!tma_warp && !p.w_sf_tiled) {
           const uint8_t* src_k = lane_sf + ks * (TR::kKPerStage / 32);
           const uint32_t dst_k = st + kSfbOff + (uint32_t)lane * 16u;
 #pragma unroll
           for (int j = 0; j < 8 * kAtomsPerStage; ++j) {
             const int jj = j & 7, ka = j >> 3;
             if (ka < katoms)
-              cp_async_4(dst_k + ka * 1024 + (jj >> 2) * 512 + (jj & 3) * 4, src_k + jj * sf_row32 + ka * 4);
+              cp_async_4(dst_k + (jj >> 2) * (kAtomsPerStage * 512) + ka * 512 + (jj & 3) * 4,
+                         src_k + jj * sf_row32 + ka * 4);
           }
+          cp_async_arrive_noinc(full_bar(slot));
         }
-        cp_async_arrive_noinc(full_bar(slot));
         armed_parity[slot] = (int)phase;
         if (++slot == kStages) {
           slot = 0;
@@ -264,8 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     }
     // Let every copy this warp started land before the CTA can exit.
     cp_async_wait_all();
-    for (int s = 0; s < kStages; ++s)
-      if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull);
+    if (tma_warp)
+      for (int s = 0; s < kStages; ++s)
+        if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull);
+  } else if (warp == kScaleWarp) {
+    // prepacked weight scales arrive with the TMA warp's bulk copies: nothing to do
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     int slot = 0;
@@ -295,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 #pragma unroll
             for (int na = 0; na < 2; ++na)
               tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8 + na * 4,
-                                   smem_desc(st + kSfbOff + ka * 1024 + na * 512, 128, 128, kLayoutNone));
+                                   smem_desc(st + kSfbOff + na * (kAtomsPerStage * 512) + ka * 512, 128, 128,
+                                             kLayoutNone));
           }
 #pragma unroll
           for (int j = 0; j < kMmaPerStage; ++j) {
@@ -463,6 +485,7 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   }
   p.act_sf = a.act_sf;
   p.w_sf = a.w_sf;
+  p.w_sf_tiled = a.w_sf_tiled;
   p.counts = a.counts;
   p.padded_offsets = a.padded_offsets;
   p.mtile_base = a.mtile_base;

@@ -124,14 +124,15 @@ constexpr int kForwardKernels = 7;  // route, scan, scatter, quant, gemm1, gemm2
 
 moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2,
                      const uint8_t* w2s, void* out, int64_t T, int H, int I, int E, int k, void* ws,
-                     size_t ws_bytes, void* stream, moe_act_fmt_t fmt, cudaEvent_t* ev = nullptr) {
+                     size_t ws_bytes, void* stream, moe_act_fmt_t fmt, bool tiled_scales,
+                     cudaEvent_t* ev = nullptr) {
   // with T == 0 nothing is read or written, so empty x / logits / out may be null
   if ((T > 0 && (!x || !logits || !out)) || !w1 || !w1s || !w2 || !w2s || !ws) return MOE_ERR_INVALID_ARG;
   moe_workspace_layout_t L;
   moe_status_t st = layout(T, H, I, E, k, fmt, &L);
   if (st != MOE_OK) return st;
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(logits, 4) || !aligned(w1, 32) || !aligned(w2, 32) ||
-      !aligned(w1s, 4) || !aligned(w2s, 4) || !aligned(ws, 256))
+      !aligned(w1s, tiled_scales ? 16 : 4) || !aligned(w2s, tiled_scales ? 16 : 4) || !aligned(ws, 256))
     return MOE_ERR_MISALIGNED;
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (T == 0) return MOE_OK;
@@ -179,6 +180,7 @@ moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, cons
   g1.rows_cap = L.rows_cap;
   g1.w = w1;
   g1.w_sf = w1s;
+  g1.w_sf_tiled = tiled_scales ? 1 : 0;
   g1.E = E;
   g1.N = 2 * I;
   g1.K = H;
@@ -307,13 +309,37 @@ moe_status_t moe_quantize_mx(const void* x, int64_t rows, int K, moe_act_fmt_t f
 moe_status_t moe_a8w4_forward(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
                               const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I, int E, int k,
                               void* ws, size_t ws_bytes, void* stream) {
-  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP8);
+  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP8, false);
+}
+
+moe_status_t moe_a8w4_forward_prepacked(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
+                                        const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I,
+                                        int E, int k, void* ws, size_t ws_bytes, void* stream) {
+  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP8, true);
+}
+
+moe_status_t moe_a4w4_forward_prepacked(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
+                                        const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I,
+                                        int E, int k, void* ws, size_t ws_bytes, void* stream) {
+  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP4, true);
+}
+
+moe_status_t moe_prepack_scales(const uint8_t* scales, int64_t rows, int K, uint8_t* tiled, void* stream) {
+  if (!scales || !tiled || rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(scales, 4) || !aligned(tiled, 16)) return MOE_ERR_MISALIGNED;
+  if (rows == 0) return MOE_OK;
+  DeviceInfo dev;
+  const moe_status_t st = device_info(&dev);
+  if (st != MOE_OK) return st;
+  MOE_CUDA_TRY(moe::launch_prepack_scales(scales, rows, K, tiled, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
 }
 
 moe_status_t moe_a4w4_forward(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
                               const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I, int E, int k,
                               void* ws, size_t ws_bytes, void* stream) {
-  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP4);
+  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP4, false);
 }
 
 moe_status_t moe_read_device_status(const void* ws, void* stream, moe_status_t* status_out) {
@@ -333,14 +359,16 @@ int moe_forward_launch_count(int64_t T) { return T > 0 ? kForwardKernels : 0; }
 moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* logits, const uint8_t* w1,
                                  const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T,
                                  int H, int I, int E, int k, void* ws, size_t ws_bytes, void* stream,
-                                 float* kernel_us) {
+                                 int prepacked_scales, float* kernel_us) {
   if (!kernel_us) return MOE_ERR_INVALID_ARG;
   if (fmt != MOE_ACT_MXFP8 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
   cudaEvent_t ev[kForwardKernels + 1] = {};
   moe_status_t st = MOE_OK;
   for (int i = 0; i <= kForwardKernels && st == MOE_OK; ++i)
     if (cudaEventCreate(&ev[i]) != cudaSuccess) st = MOE_ERR_CUDA;
-  if (st == MOE_OK) st = forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt, ev);
+  if (st == MOE_OK)
+    st = forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt, prepacked_scales != 0,
+                 ev);
   if (st == MOE_OK && T > 0) {
     if (cudaEventSynchronize(ev[kForwardKernels]) != cudaSuccess) st = MOE_ERR_CUDA;
     for (int i = 0; i < kForwardKernels && st == MOE_OK; ++i) {

@@ -71,6 +71,8 @@ struct QuantArgs {
   int k;
 };
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
+// Canonical [rows, K/32] scales -> 128x4 tile layout (rows % 128 == 0, K % 128 == 0).
+cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst, cudaStream_t s);
 
 // gemm.cu
 struct GemmArgs {
@@ -80,7 +82,8 @@ struct GemmArgs {
   const uint8_t* act_sf;  // [rows_cap/128][K/128][512]
   int64_t rows_cap;
   const uint8_t* w;       // MXFP4 [E, N, K/2]
-  const uint8_t* w_sf;    // E8M0 [E, N, K/32]
+  const uint8_t* w_sf;    // E8M0 [E, N, K/32], or its 128x4 tile layout when w_sf_tiled
+  int w_sf_tiled;
   int E, N, K;
   const int32_t* counts;
   const int64_t* padded_offsets;

@@ -81,7 +81,28 @@ __global__ void __launch_bounds__(kQuantThreads) quant_kernel(QuantArgs a) {
   }
 }
 
+// Canonical E8M0 scales [rows, K/32] -> the 128x4 tile layout the GEMM copies to TMEM:
+// thread i moves the 4 scale bytes (one 128-wide k-atom) of one row.
+__global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* src, int64_t rows, int K, uint8_t* dst) {
+  const int groups = K / 128;
+  const int64_t n = rows * groups;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / groups;
+    const int g = (int)(i % groups);
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(src + r * (K / 32) + 4 * g);
+    *reinterpret_cast<uint32_t*>(dst + ((r >> 7) * groups + g) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4) = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst, cudaStream_t s) {
+  const int64_t n = rows * (K / 128);
+  if (n == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
+  prepack_scales_kernel<<<grid, 256, 0, s>>>(src, rows, K, dst);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
   const int col_blocks = (a.K + kColsPerBlock - 1) / kColsPerBlock;

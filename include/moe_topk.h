@@ -220,6 +220,34 @@ moe_status_t moe_a4w4_forward(const void* x_bf16, const float* gate_logits, cons
                               size_t workspace_bytes, void* stream);
 
 /*
+ * One-time rearrangement of MXFP4 weight scales for the *_prepacked forwards, the
+ * analogue of the load-time scale shuffle of "feat(moe): FlyDSL MegaMoE fused EP-MoE
+ * integration" (description: shuffle_scale_w4 for w1/w1_scale).  Only the scale bytes
+ * move; the FP4 codes stay in their canonical layout.
+ *   scales  E8M0 [rows, K/32] row-major in, device, 4-byte aligned (rows = E*2I for W1,
+ *           E*H for W2; K = H for W1, I for W2)
+ *   tiled   out, device, 16-byte aligned, rows*K/32 bytes: the 128x4 tile layout, the
+ *           scale of (row r, 32-block kb) at ((r/128)*(K/128) + kb/4)*512 + (r%32)*16 +
+ *           ((r%128)/32)*4 + kb%4
+ *   rows % 128 == 0 and K % 128 == 0, else MOE_ERR_UNSUPPORTED_SHAPE.
+ */
+moe_status_t moe_prepack_scales(const uint8_t* scales, int64_t rows, int K, uint8_t* tiled, void* stream);
+
+/*
+ * moe_a8w4_forward / moe_a4w4_forward with w1_scale and w2_scale already in the tile
+ * layout of moe_prepack_scales (16-byte aligned).  Identical results; the weight scales
+ * then stream with two 512-byte bulk copies per pipeline stage instead of 4-byte gathers.
+ */
+moe_status_t moe_a8w4_forward_prepacked(const void* x_bf16, const float* gate_logits, const uint8_t* w1,
+                                        const uint8_t* w1_scale_tiled, const uint8_t* w2,
+                                        const uint8_t* w2_scale_tiled, void* out_bf16, int64_t T, int H, int I,
+                                        int E, int k, void* workspace, size_t workspace_bytes, void* stream);
+moe_status_t moe_a4w4_forward_prepacked(const void* x_bf16, const float* gate_logits, const uint8_t* w1,
+                                        const uint8_t* w1_scale_tiled, const uint8_t* w2,
+                                        const uint8_t* w2_scale_tiled, void* out_bf16, int64_t T, int H, int I,
+                                        int E, int k, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Read the device status word a forward (or sort) left in `workspace`.
  * Synchronises `stream`, then copies 4 bytes to the host.  *status_out gets
  * MOE_OK or the moe_status_t a kernel recorded (MOE_ERR_DEVICE_TIMEOUT,
@@ -232,7 +260,8 @@ int moe_forward_launch_count(int64_t T);
 
 /*
  * Profiling form of the forward: enqueues exactly the launch sequence of
- * moe_a8w4_forward (fmt = MOE_ACT_MXFP8) or moe_a4w4_forward (MOE_ACT_MXFP4)
+ * moe_a8w4_forward (fmt = MOE_ACT_MXFP8) or moe_a4w4_forward (MOE_ACT_MXFP4),
+ * or of their *_prepacked forms when prepacked_scales != 0,
  * with a CUDA event recorded before the first kernel and after each kernel,
  * waits for the last event, and writes the duration of each kernel in
  * microseconds to kernel_us[moe_forward_launch_count(T)] (HOST array), in
@@ -244,7 +273,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x_bf16, const fl
                                  const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
                                  const uint8_t* w2_scale, void* out_bf16, int64_t T, int H, int I, int E,
                                  int k, void* workspace, size_t workspace_bytes, void* stream,
-                                 float* kernel_us);
+                                 int prepacked_scales, float* kernel_us);
 
 #ifdef __cplusplus
 }

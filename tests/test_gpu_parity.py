@@ -292,3 +292,37 @@ def test_profile_forward_matches_forward():
     torch.cuda.synchronize()
     assert list(us) == list(moe.KERNEL_NAMES) and all(v > 0 for v in us.values())
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+# --------------------------------------------------------------------------- prepacked scales
+def _prepack(t):
+    out = torch.empty_like(t)
+    moe.moe_prepack_scales(t, out)
+    return out
+
+
+def test_prepack_scales_layout():
+    rows, K = 384, 640
+    sc = torch.randint(0, 255, (rows, K // 32), dtype=torch.uint8, device=DEV)
+    tiled = _prepack(sc).cpu().numpy().reshape(-1)
+    assert np.array_equal(tile_sf_to_rows(tiled, rows, K), sc.cpu().numpy())
+
+
+@pytest.mark.parametrize("shape,T,act", [("tiny", 16, moe.MOE_ACT_MXFP8), ("tiny", 16, moe.MOE_ACT_MXFP4),
+                                         ("flash_decode", 64, moe.MOE_ACT_MXFP8), ("draft", 300, moe.MOE_ACT_MXFP8),
+                                         ("pro", 512, moe.MOE_ACT_MXFP8), ("pro", 512, moe.MOE_ACT_MXFP4)])
+def test_forward_prepacked_is_bit_identical(shape, T, act):
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 2).to(DEV), synth.gate_logits(T, s.E, 2, skew=s.skew).to(DEV)
+    w1, w1s, w2, w2s = W.dev
+    out_a = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+    out_b = torch.empty_like(out_a)
+    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act), dtype=torch.uint8, device=DEV)
+    fwd = moe.moe_a8w4_forward if act == moe.MOE_ACT_MXFP8 else moe.moe_a4w4_forward
+    fwd_p = moe.moe_a8w4_forward_prepacked if act == moe.MOE_ACT_MXFP8 else moe.moe_a4w4_forward_prepacked
+    fwd(x, lg, w1, w1s, w2, w2s, out_a, s.E, s.k, ws)
+    fwd_p(x, lg, w1, _prepack(w1s), w2, _prepack(w2s), out_b, s.E, s.k, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
