@@ -238,5 +238,5 @@ def workspace_views(workspace, T, H, I, E, k, fmt=MOE_ACT_MXFP8):
         sorted_pair=v(L.sorted_pair, R, torch.int32), inv=v(L.inv, R, torch.int32),
         inv_padded=v(L.inv_padded, R, torch.int32), xq=v(L.xq, rc * hb, torch.uint8).view(rc, hb),
         xs=v(L.xs, rc * H // 32, torch.uint8), a2=v(L.a2, rc * ib, torch.uint8).view(rc, ib),
-        a2s=v(L.a2s, rc * I // 32, torch.uint8), y2=v(L.y2, rc * H, torch.float32).view(rc, H),
+        a2s=v(L.a2s, rc * I // 32, torch.uint8), y2=v(L.y2, rc * H, torch.bfloat16).view(rc, H),
         status=v(L.status, 8, torch.int32))

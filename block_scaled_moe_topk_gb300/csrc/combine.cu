@@ -2,8 +2,8 @@
 //
 // out[t, n] = bf16_rne( sum_{j<k} topk_w[t, j] * y2[inv_padded[t*k + j], n] ), accumulated in
 // fp32 in slot order ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical
-// Details: "accumulate TopK contributions in FP32").  Each thread owns 8 consecutive
-// columns: two 16-byte loads per slot, one 16-byte bf16 store.
+// Details: "accumulate TopK contributions in FP32"); y2 rows are bf16.  Each thread owns 8
+// consecutive columns: one 16-byte load per slot, one 16-byte bf16 store.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -27,16 +27,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
     for (int j = 0; j < k; ++j) {
       const float w = a.w[t * k + j];
-      const float4* src = reinterpret_cast<const float4*>(a.y2 + (int64_t)a.inv_padded[t * k + j] * H + c0);
-      const float4 v0 = src[0], v1 = src[1];
-      acc[0] = fmaf(w, v0.x, acc[0]);
-      acc[1] = fmaf(w, v0.y, acc[1]);
-      acc[2] = fmaf(w, v0.z, acc[2]);
-      acc[3] = fmaf(w, v0.w, acc[3]);
-      acc[4] = fmaf(w, v1.x, acc[4]);
-      acc[5] = fmaf(w, v1.y, acc[5]);
-      acc[6] = fmaf(w, v1.z, acc[6]);
-      acc[7] = fmaf(w, v1.w, acc[7]);
+      const uint4 raw = *reinterpret_cast<const uint4*>(a.y2 + (int64_t)a.inv_padded[t * k + j] * H + c0);
+      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[2 * c] = fmaf(w, __uint_as_float(u[c] << 16), acc[2 * c]);              // low half: column c0+2c
+        acc[2 * c + 1] = fmaf(w, __uint_as_float(u[c] & 0xFFFF0000u), acc[2 * c + 1]);
+      }
     }
     uint32_t packed[4];
 #pragma unroll

@@ -6,13 +6,14 @@
 //                  INTERLEAVE(g1u1)); the epilogue forms h_j = silu(gate_j) * up_j and requantises
 //                  h to MX (A2: "add A4W4 and FP8 P2P transport support to MegaMoE", Technical
 //                  Details: "emit FP4 A2 activations/scales"; E4M3 codes for A8W4).
-//   GEMM2 (EPI=1): y2[r, n] = sum_I a2[r, I] * W2[e, n, I], stored as fp32 rows.
+//   GEMM2 (EPI=1): y2[r, n] = sum_I a2[r, I] * W2[e, n, I], accumulated in fp32, stored as bf16.
 //
 // Tiles are 128 routed rows (one expert's padded segment) x 256 output columns.  Per CTA:
 //   warp 0      producer: TMA (activation tile 128x128B, weight tile 256x128B) and a bulk copy
 //               of the activation scales (already in the 128x4 tile layout);
-//   warp 10     producer: 4-byte cp.async copies that rearrange the canonical weight scales
-//               into that layout, in parallel with warp 0;
+//   warp 10     producer: with canonical weight scales, 4-byte cp.async copies that rearrange
+//               them into that layout; with prepacked scales, the TMA of the weight tile and
+//               the bulk copies of its scales (so the two halves of a stage issue in parallel);
 //   warp 1      TMEM owner and MMA issuer (one thread): tcgen05.cp of the scales to TMEM, then
 //               tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1, scale_vec 1X) or kind::mxf4 (E2M1 x E2M1,
 //               scale_vec 2X) into a 128x256 fp32 accumulator in TMEM;
@@ -27,6 +28,7 @@
 // pace of an earlier version): barrier probes are inlined, addressing is hoisted per tile.  Every wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
 // status word, lets its own copies and MMAs drain (again bounded), frees TMEM and returns.
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 #include <mutex>
 
@@ -62,7 +64,7 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   const int32_t* mtile_base;
   uint8_t* out_codes;
   uint8_t* out_sf;
-  float* out_f32;
+  uint16_t* out_bf16;
   uint32_t* status;
   uint64_t timeout_ns;
   int E, N, K;
@@ -126,23 +128,30 @@ struct Sync {
 };
 
 // Poll a phase of an mbarrier until it completes, the CTA aborts, or the time limit passes.
+// The limit is counted in SM clock cycles (clock64 is cheap; %globaltimer is not), at 2
+// cycles per nanosecond of limit_ns, so at any SM clock >= 1 GHz the wait ends within
+// 2 x limit_ns.  No clock is read during the first 64 probes, which is where a phase that
+// is merely a little late completes.
 __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t limit_cycles = 2 * limit_ns;
+  uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (*s.abort_flag) return false;
-      const uint64_t dt = global_timer_ns() - t0;
-      if (dt > limit_ns) {
+      const uint64_t now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > limit_cycles) {
         *s.abort_flag = 1;
         atomicOr(s.status, kStatusTimeout);
-        // first expiry only: barrier index, parity, CTA, warp, microseconds waited
+        // first expiry only: barrier index, parity, CTA, warp, microseconds waited (at 2 GHz)
         if (atomicCAS(s.status + 1, 0u, 1u) == 0u) {
           s.status[2] = (bar - s.bar0) / 8;
           s.status[3] = parity;
           s.status[4] = blockIdx.x;
           s.status[5] = threadIdx.x / 32;
-          s.status[6] = (uint32_t)(dt / 1000);
+          s.status[6] = (uint32_t)((now - t0) / 2000);
         }
         return false;
       }
@@ -186,8 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // TMA warp's expect_tx arrive (+ 32 cp.async arrivals of the scale warp for canonical scales)
-      mbar_init(full_bar(s), p.w_sf_tiled ? 1 : 1 + 32);
+      // canonical scales: warp 0's expect_tx arrive + 32 cp.async arrivals of the scale warp;
+      // prepacked scales: one expect_tx arrive from each of warps 0 and 10
+      mbar_init(full_bar(s), p.w_sf_tiled ? 2 : 1 + 32);
       mbar_init(empty_bar(s), 1);      // tcgen05.commit
     }
     mbar_init(tmem_full_bar, 1);
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const int nks = (K + TR::kKPerStage - 1) / TR::kKPerStage;
   const int64_t total_tiles = (int64_t)p.mtile_base[p.E] * NT;
 
-  if (warp == 0 || (warp == kScaleWarp && !p.w_sf_tiled)) {
+  if (warp == 0 || warp == kScaleWarp) {
     // ------------------------------------------------------------------ producers
     // Warp 0 issues the TMA loads of a stage; warp 10 gathers the stage's weight scales
     // with 4-byte cp.async copies.  Both walk the same stages and wait for the same free
@@ -243,15 +253,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         }
         const int katoms = min(TR::kKPerStage, K - ks * TR::kKPerStage) / 128;
         const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
-        if (tma_warp && lane == 0) {
-          mbar_arrive_expect_tx(full_bar(slot),
-                                (uint32_t)(kABytes + TR::kBTxBytes + katoms * 512 + (p.w_sf_tiled ? 2 * katoms * 512 : 0)));
-          tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
-          tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
-          bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
-                    (uint32_t)katoms * 512u, full_bar(slot));
-          if (p.w_sf_tiled) {
-            // prepacked weight scales: one contiguous run of k-atoms per 128-row half of the tile
+        if (lane == 0) {
+          if (tma_warp) {
+            // activation side, plus the weight codes when the scale warp is busy gathering
+            mbar_arrive_expect_tx(full_bar(slot),
+                                  (uint32_t)(kABytes + katoms * 512 + (p.w_sf_tiled ? 0 : TR::kBTxBytes)));
+            tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
+            bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
+                      (uint32_t)katoms * 512u, full_bar(slot));
+            if (!p.w_sf_tiled) tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
+          } else if (p.w_sf_tiled) {
+            // weight side with prepacked scales: codes + one contiguous run of k-atoms per
+            // 128-row half of the tile, issued in parallel with warp 0
+            mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(TR::kBTxBytes + 2 * katoms * 512));
+            tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
 #pragma unroll
             for (int na = 0; na < 2; ++na)
               bulk_load(st + kSfbOff + na * (kAtomsPerStage * 512),
@@ -285,8 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     if (tma_warp)
       for (int s = 0; s < kStages; ++s)
         if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull);
-  } else if (warp == kScaleWarp) {
-    // prepacked weight scales arrive with the TMA warp's bulk copies: nothing to do
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     int slot = 0;
@@ -404,9 +417,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           }
         }
       } else if (valid) {
-        float4* d4 = reinterpret_cast<float4*>(p.out_f32 + prow * p.N + tc.nt * kNTile + half * 128);
+        // GEMM2 rows stored as bf16 (round to nearest even); the combine accumulates in fp32
+        uint4* d4 = reinterpret_cast<uint4*>(p.out_bf16 + prow * p.N + tc.nt * kNTile + half * 128);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) d4[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        for (int i = 0; i < 16; ++i) {
+          uint32_t w[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * i + 2 * c], acc[8 * i + 2 * c + 1]);
+            w[c] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
     }
   }
@@ -491,7 +513,7 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   p.mtile_base = a.mtile_base;
   p.out_codes = a.out_codes;
   p.out_sf = a.out_sf;
-  p.out_f32 = a.out_f32;
+  p.out_bf16 = a.out_bf16;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   p.E = a.E;

@@ -93,7 +93,7 @@ moe_status_t layout(int64_t T, int H, int I, int E, int k, moe_act_fmt_t fmt, mo
   L->xs = take((size_t)H / 32 * rows_cap);
   L->a2 = take(ib * rows_cap);
   L->a2s = take((size_t)I / 32 * rows_cap);
-  L->y2 = take(sizeof(float) * (size_t)H * rows_cap);
+  L->y2 = take(sizeof(uint16_t) * (size_t)H * rows_cap);
   L->total = off;
   L->rows_cap = rows_cap;
   L->nchunk = nchunk;
@@ -208,11 +208,11 @@ moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, cons
   g2.max_tiles = mtiles_cap * (H / moe::kNTile);
   g2.out_codes = nullptr;
   g2.out_sf = nullptr;
-  g2.out_f32 = reinterpret_cast<float*>(at(L.y2));
+  g2.out_bf16 = reinterpret_cast<uint16_t*>(at(L.y2));
   MOE_CUDA_TRY(moe::launch_gemm(g2, s));
   MOE_CUDA_TRY(mark());
 
-  moe::CombineArgs ca{reinterpret_cast<const float*>(at(L.y2)), tw, inv_padded, T, H, k, static_cast<uint16_t*>(out)};
+  moe::CombineArgs ca{reinterpret_cast<const uint16_t*>(at(L.y2)), tw, inv_padded, T, H, k, static_cast<uint16_t*>(out)};
   MOE_CUDA_TRY(moe::launch_combine(ca, s));
   MOE_CUDA_TRY(mark());
   return MOE_OK;

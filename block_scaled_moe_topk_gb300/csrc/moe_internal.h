@@ -91,7 +91,7 @@ struct GemmArgs {
   int64_t max_tiles;      // host upper bound on tiles (grid sizing)
   uint8_t* out_codes;     // GEMM1: A2 codes [rows_cap, N/2 or N/4]
   uint8_t* out_sf;        // GEMM1: A2 scales, 128x4 tile layout over N/2 columns
-  float* out_f32;         // GEMM2: y2 [rows_cap, N]
+  uint16_t* out_bf16;     // GEMM2: y2 bf16 [rows_cap, N]
   uint32_t* status;
   uint64_t timeout_ns;
   int num_sms;
@@ -100,7 +100,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 
 // combine.cu
 struct CombineArgs {
-  const float* y2;          // [rows_cap, H]
+  const uint16_t* y2;       // bf16 [rows_cap, H]
   const float* w;           // [T, k]
   const int32_t* inv_padded;
   int64_t T;

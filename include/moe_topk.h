@@ -102,7 +102,9 @@ const char* moe_status_string(moe_status_t status);
  *   xs           u8 [rows_cap/128][H/128][512]  their E8M0 scales, 128x4 tile layout
  *   a2           u8 [rows_cap, I or I/2]   requantised SwiGLU output codes
  *   a2s          u8 [rows_cap/128][I/128][512]  their scales, same tile layout
- *   y2           fp32 [rows_cap, H]        GEMM2 output rows (unweighted)
+ *   y2           bf16 [rows_cap, H]        GEMM2 output rows (unweighted; fp32-accumulated,
+ *                                          rounded to bf16 like the pages' reduced-precision
+ *                                          stage-2 transport)
  *   status       uint32[8]: [0] device status bits (read them with moe_read_device_status);
  *                [1..6] the first expired in-kernel wait, if any: [1] = 1 when recorded,
  *                [2] barrier index, [3] phase parity, [4] CTA, [5] warp, [6] microseconds waited
