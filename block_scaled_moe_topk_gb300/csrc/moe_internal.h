@@ -98,6 +98,7 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 
+
 // combine.cu
 struct CombineArgs {
   const uint16_t* y2;       // bf16 [rows_cap, H]
