@@ -70,6 +70,7 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   uint64_t timeout_ns;
   int E, N, K;
   int w_sf_tiled;
+  int test_stall;
 };
 
 template <int ACT>
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     int armed_parity[kStages];
 #pragma unroll
     for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
-    bool ok = true;
+    bool ok = !p.test_stall;  // the test hook leaves every stage unfilled
     for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       const Tile tc = decode_tile(tile, p.mtile_base, p.E, NT);
       const int64_t row0 = p.padded_offsets[tc.e] + (int64_t)tc.mt * kRowTile;
@@ -223,9 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     }
     // Let every copy this warp started land before the CTA can exit.
     cp_async_wait_all();
-    if (tma_warp)
+    // both warps that issued TMA / bulk copies (warp 10 does with prepacked scales) let
+    // them land before the CTA can exit
+    if (tma_warp || p.w_sf_tiled)
       for (int s = 0; s < kStages; ++s)
-        if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull);
+        if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull, true);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     int slot = 0;
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     if (issued) {
       if (lane == 0) tc_commit(drain_bar);
       __syncwarp();
-      warp_wait(drain_bar, 0, sync, 100000000ull);
+      warp_wait(drain_bar, 0, sync, 100000000ull, true);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -416,6 +419,7 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   p.act_sf = a.act_sf;
   p.w_sf = a.w_sf;
   p.w_sf_tiled = a.w_sf_tiled;
+  p.test_stall = a.test_stall;
   p.counts = a.counts;
   p.padded_offsets = a.padded_offsets;
   p.mtile_base = a.mtile_base;

@@ -48,13 +48,16 @@ struct Sync {
 // cycles per nanosecond of limit_ns, so at any SM clock >= 1 GHz the wait ends within
 // 2 x limit_ns.  No clock is read during the first 64 probes, which is where a phase that
 // is merely a little late completes.
-__device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns) {
+// With drain = true the abort flag is ignored: used at exit to let this CTA's own copies and
+// MMAs land (bounded by limit_ns alone) before TMEM is freed.
+__device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns,
+                                          bool drain = false) {
   const uint64_t limit_cycles = 2 * limit_ns;
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 63u) {
-      if (*s.abort_flag) return false;
+      if (!drain && *s.abort_flag) return false;
       const uint64_t now = clock64();
       if (t0 == 0) {
         t0 = now;
@@ -80,10 +83,11 @@ __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const S
 // while another one is leaving on the abort path.
 // The common case (the phase already completed) costs one probe and one vote; the timed
 // polling loop only runs after a miss.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns,
+                                          bool drain = false) {
   bool ok = mbar_try_wait(bar, parity);
   if (__all_sync(0xffffffffu, ok)) return true;
-  if (!ok) ok = bounded_wait(bar, parity, s, limit_ns);
+  if (!ok) ok = bounded_wait(bar, parity, s, limit_ns, drain);
   return __all_sync(0xffffffffu, ok);
 }
 

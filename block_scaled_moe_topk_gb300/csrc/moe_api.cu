@@ -113,6 +113,18 @@ uint64_t wait_timeout_ns() {
   return v;
 }
 
+// Test hook for the failure path: MOE_TEST_STALL_PRODUCER=1 makes the GEMM producers issue
+// nothing, so the first wait of the MMA warp expires after MOE_WAIT_TIMEOUT_NS and the kernel
+// reports MOE_ERR_DEVICE_TIMEOUT through the workspace status words (no fault, no hang).
+int test_stall_producer() {
+  static int v = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    if (const char* s = getenv("MOE_TEST_STALL_PRODUCER")) v = atoi(s) != 0;
+  });
+  return v;
+}
+
 #define MOE_CUDA_TRY(expr)                          \
   do {                                              \
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
@@ -193,6 +205,7 @@ moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, cons
   g1.status = status;
   g1.timeout_ns = wait_timeout_ns();
   g1.num_sms = dev.num_sms;
+  g1.test_stall = test_stall_producer();
   cudaError_t err = moe::launch_gemm(g1, s);
   MOE_CUDA_TRY(err);
   MOE_CUDA_TRY(mark());

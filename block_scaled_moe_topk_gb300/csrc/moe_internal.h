@@ -95,6 +95,7 @@ struct GemmArgs {
   uint32_t* status;
   uint64_t timeout_ns;
   int num_sms;
+  int test_stall;         // test hook: the producer issues nothing, so the MMA warp's wait expires
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 

@@ -74,15 +74,30 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
         my_val = bv;
       }
     }
-    // exp of the exact difference (a difference of two floats is exact in double): only k
-    // values per token, so the fp64 exp costs nothing measurable
-    const double p = (lane < k) ? exp((double)my_val - (double)lmax) : 0.0;
-    double z = p;
+    // p_j = exp(l_j - l_max) without fp64 (scarce on this GPU): the difference is split
+    // exactly into s + e (two-sum), so its rounding is not amplified by exp, and
+    // exp(s + e) = expf(s) * (1 + e) because |e| <= ulp(s) / 2.
+    float p = 0.0f;
+    if (lane < k) {
+      const float sdiff = my_val - lmax;
+      const float bb = sdiff - my_val;
+      const float e = (my_val - (sdiff - bb)) + (-lmax - bb);
+      p = expf(sdiff) * (1.0f + e);
+    }
+    // z = sum of the k values as a compensated (hi, lo) pair, so w = p / z loses <= 1 ulp
+    float zh = p, zl = 0.0f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    for (int off = 16; off > 0; off >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, zh, off);
+      const float ol = __shfl_xor_sync(0xffffffffu, zl, off);
+      const float sum = zh + oh;
+      const float bv = sum - zh;
+      zl += ol + ((zh - (sum - bv)) + (oh - bv));
+      zh = sum;
+    }
     if (lane < k) {
       a.ids[t * k + lane] = my_id;
-      a.w[t * k + lane] = (float)(p / z);
+      a.w[t * k + lane] = __fdiv_rn(p, zh) * (1.0f - __fdiv_rn(zl, zh));
       if (a.chunk_hist) atomicAdd(&hist[my_id], 1);
     }
   }

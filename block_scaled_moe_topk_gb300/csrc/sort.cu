@@ -53,16 +53,26 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(SortArgs a) {
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   const int E = a.E;
   const int64_t nchunk = a.nchunk;
-  // per expert: exclusive prefix over chunks, in place
+  // per expert: exclusive prefix over chunks, in place; 8 rows of 32 chunks are loaded
+  // before any is scanned so the loads overlap instead of forming a latency chain
+  constexpr int kRounds = 8;
   for (int e = warp; e < E; e += kScanThreads / 32) {
     int32_t* col = a.chunk_hist + (int64_t)e * nchunk;
     int running = 0;
-    for (int64_t b0 = 0; b0 < nchunk; b0 += 32) {
-      const int64_t b = b0 + lane;
-      const int v = (b < nchunk) ? col[b] : 0;
-      const int incl = warp_inclusive_scan<int>(v, lane);
-      if (b < nchunk) col[b] = running + incl - v;
-      running += __shfl_sync(0xffffffffu, incl, 31);
+    for (int64_t b0 = 0; b0 < nchunk; b0 += 32 * kRounds) {
+      int v[kRounds];
+#pragma unroll
+      for (int r = 0; r < kRounds; ++r) {
+        const int64_t b = b0 + 32 * r + lane;
+        v[r] = (b < nchunk) ? col[b] : 0;
+      }
+#pragma unroll
+      for (int r = 0; r < kRounds; ++r) {
+        const int64_t b = b0 + 32 * r + lane;
+        const int incl = warp_inclusive_scan<int>(v[r], lane);
+        if (b < nchunk) col[b] = running + incl - v[r];
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
     if (lane == 0) cnt[e] = running;
   }

@@ -51,6 +51,9 @@
  *     kernel) are recorded in a status word inside the workspace; read it with
  *     moe_read_device_status after the stream has finished.
  *   - No call throws, traps or aborts.  Kernels never __trap().
+ *   - Environment (read once per process): MOE_WAIT_TIMEOUT_NS bounds every in-kernel wait
+ *     (default 4 s); MOE_TEST_STALL_PRODUCER=1 is a test hook that makes the GEMM producers
+ *     issue nothing, so a forward ends with MOE_ERR_DEVICE_TIMEOUT in its status word.
  *   - The forward calls may be captured into a CUDA graph; a captured graph is
  *     valid only for the pointers and sizes it was captured with.
  *   - Supported device: compute capability 10.3 (sm_103a) only.

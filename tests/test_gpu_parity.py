@@ -212,13 +212,13 @@ def _sampled_check(act, s, T, n_sample, seed=0):
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
 
 
-@pytest.mark.parametrize("T", [1, 64, 3072])
+@pytest.mark.parametrize("T", [1, 64, 77, 3072])
 def test_forward_draft_skewed(T):
     _sampled_check(moe.MOE_ACT_MXFP8, synth.SHAPES["draft"], T, 48)
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("T,skew", [(1, False), (128, False), (8192, False), (8192, True)])
+@pytest.mark.parametrize("T,skew", [(1, False), (128, False), (8192, False), (8192, True), (32768, False)])
 def test_forward_pro_a8w4(T, skew):
     s = synth.SHAPES["pro_skew" if skew else "pro"]
     _sampled_check(moe.MOE_ACT_MXFP8, s, T, 24)
@@ -326,3 +326,15 @@ def test_forward_prepacked_is_bit_identical(shape, T, act):
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+def test_forward_api_limits_1024_experts_top8():
+    """The largest expert count and top-k the API takes, with a small hidden size."""
+    E, k, H, I, T = 1024, 8, 256, 128, 100
+    W = Weights(E, H, I, seed=5, device=DEV)
+    x, lg = synth.x_bf16(T, H, 5), synth.gate_logits(T, E, 5)
+    out, ws = _run_forward(moe.MOE_ACT_MXFP8, x, lg, W, E, k)
+    _check_intermediates(moe.MOE_ACT_MXFP8, x, lg, W, E, k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, oracle.FMT_E4M3)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
