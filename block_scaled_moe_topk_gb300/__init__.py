@@ -17,7 +17,7 @@ __all__ = [
     "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
     "moe_quantize_mx", "moe_a8w4_forward",
-    "moe_a4w4_forward", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
+    "moe_a4w4_forward", "moe_forward_ex", "moe_a8w4_forward_prequant", "moe_a4w4_forward_prequant", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
     "moe_read_device_status", "moe_forward_launch_count", "moe_profile_forward",
     "workspace_views",
 ]
@@ -43,6 +43,15 @@ class WorkspaceLayout(ctypes.Structure):
         "status", "topk_ids", "topk_w", "counts", "offsets", "padded_offsets", "mtile_base", "chunk_hist",
         "sorted_pair", "inv", "inv_padded", "xq", "xs", "a2", "a2s", "y2", "total")] + [
         ("rows_cap", ctypes.c_int64), ("nchunk", ctypes.c_int64)]
+
+
+class ForwardArgs(ctypes.Structure):
+    _fields_ = [("act_fmt", ctypes.c_int), ("prequantized", ctypes.c_int), ("weight_scales_prepacked", ctypes.c_int),
+                ("x", ctypes.c_void_p), ("x_scale", ctypes.c_void_p), ("gate_logits", ctypes.c_void_p),
+                ("w1", ctypes.c_void_p), ("w1_scale", ctypes.c_void_p), ("w2", ctypes.c_void_p),
+                ("w2_scale", ctypes.c_void_p), ("out", ctypes.c_void_p), ("T", ctypes.c_int64), ("H", ctypes.c_int),
+                ("I", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p)]
 
 
 _lib = None
@@ -82,6 +91,12 @@ def lib():
     L.moe_profile_forward.restype = i32
     L.moe_profile_forward.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P, i32,
                                       ctypes.POINTER(ctypes.c_float)]
+    for name in ("moe_a8w4_forward_prequant", "moe_a4w4_forward_prequant"):
+        f = getattr(L, name)
+        f.restype = i32
+        f.argtypes = [P, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P]
+    L.moe_forward_ex.restype = i32
+    L.moe_forward_ex.argtypes = [ctypes.POINTER(ForwardArgs)]
     L.moe_prepack_scales.restype = i32
     L.moe_prepack_scales.argtypes = [P, i64, i32, P, P]
     _lib = L
@@ -174,6 +189,43 @@ def moe_a4w4_forward(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, work
     _forward("moe_a4w4_forward", x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream)
 
 
+def _forward_prequant(name, xq, xq_scale, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream):
+    T, H = out.shape
+    I = w2.shape[-1] * 2
+    f = getattr(lib(), name)
+    _check(f(_p(xq), _p(xq_scale), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale), _p(out), T, H, I,
+             int(E), int(k), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)), name)
+
+
+def moe_a8w4_forward_prequant(xq, xq_scale, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace,
+                              stream=None):
+    """The A8W4 layer from prequantised activations: xq u8 [T, H] E4M3, xq_scale u8 [T, H/32]."""
+    _forward_prequant("moe_a8w4_forward_prequant", xq, xq_scale, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k,
+                      workspace, stream)
+
+
+def moe_a4w4_forward_prequant(xq, xq_scale, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace,
+                              stream=None):
+    """The A4W4 layer from prequantised activations: xq u8 [T, H/2] E2M1, xq_scale u8 [T, H/32]."""
+    _forward_prequant("moe_a4w4_forward_prequant", xq, xq_scale, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k,
+                      workspace, stream)
+
+
+def moe_forward_ex(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, act_fmt=MOE_ACT_MXFP8,
+                   x_scale=None, weight_scales_prepacked=False, stream=None):
+    """Any forward variant: bf16 x (x_scale None) or prequantised codes + scales; canonical or
+    prepacked weight scales."""
+    T, H = out.shape
+    a = ForwardArgs(act_fmt=int(act_fmt), prequantized=int(x_scale is not None),
+                    weight_scales_prepacked=int(bool(weight_scales_prepacked)), x=x.data_ptr(),
+                    x_scale=None if x_scale is None else x_scale.data_ptr(), gate_logits=gate_logits.data_ptr(),
+                    w1=w1.data_ptr(), w1_scale=w1_scale.data_ptr(), w2=w2.data_ptr(), w2_scale=w2_scale.data_ptr(),
+                    out=out.data_ptr(), T=T, H=H, I=w2.shape[-1] * 2, E=int(E), k=int(k),
+                    workspace=workspace.data_ptr(), workspace_bytes=workspace.numel() * workspace.element_size(),
+                    stream=_stream(stream).value)
+    _check(lib().moe_forward_ex(ctypes.byref(a)), "moe_forward_ex")
+
+
 def moe_prepack_scales(scales, tiled, stream=None):
     """E8M0 scales [..., rows, K/32] (any leading dims) -> 128x4 tile layout into ``tiled`` (same bytes)."""
     K = scales.shape[-1] * 32
@@ -195,6 +247,7 @@ def moe_a4w4_forward_prepacked(x, gate_logits, w1, w1_scale_tiled, w2, w2_scale_
 
 
 KERNEL_NAMES = ("route", "scan", "scatter", "quant", "gemm1", "gemm2", "combine")
+KERNEL_NAMES_SMALL = ("route_sort", "quant", "gemm1", "gemm2", "combine")  # T <= 64
 
 
 def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None,
@@ -209,7 +262,8 @@ def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E,
                                      workspace.numel() * workspace.element_size(), _stream(stream),
                                      int(bool(prepacked_scales)), us),
            "moe_profile_forward")
-    return {KERNEL_NAMES[i]: float(us[i]) for i in range(n)}
+    names = KERNEL_NAMES if n == len(KERNEL_NAMES) else KERNEL_NAMES_SMALL
+    return {names[i]: float(us[i]) for i in range(n)}
 
 
 def moe_read_device_status(workspace, stream=None) -> int:

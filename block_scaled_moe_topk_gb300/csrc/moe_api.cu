@@ -132,12 +132,17 @@ int test_stall_producer() {
 
 // The forward's launch sequence.  With `ev` (kForwardKernels + 1 events) an event is
 // recorded before the first kernel and after every kernel, for per-kernel timing.
-constexpr int kForwardKernels = 7;  // route, scan, scatter, quant, gemm1, gemm2, combine
+// T > 64: route, scan, scatter, quant, gemm1, gemm2, combine; T <= 64: route_sort, quant,
+// gemm1, gemm2, combine.
+constexpr int kForwardKernels = 7;
+int launch_count(int64_t T) { return T <= 0 ? 0 : (T <= moe::kSmallRouteTokens ? 5 : kForwardKernels); }
 
-moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2,
-                     const uint8_t* w2s, void* out, int64_t T, int H, int I, int E, int k, void* ws,
-                     size_t ws_bytes, void* stream, moe_act_fmt_t fmt, bool tiled_scales,
-                     cudaEvent_t* ev = nullptr) {
+// x is bf16 [T, H] when x_scale is null, else prequantised codes [T, H or H/2] with canonical
+// E8M0 scales x_scale [T, H/32] (the quantiser is then replaced by a permuting copy).
+moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits, const uint8_t* w1,
+                     const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H,
+                     int I, int E, int k, void* ws, size_t ws_bytes, void* stream, moe_act_fmt_t fmt,
+                     bool tiled_scales, cudaEvent_t* ev = nullptr) {
   // with T == 0 nothing is read or written, so empty x / logits / out may be null
   if ((T > 0 && (!x || !logits || !out)) || !w1 || !w1s || !w2 || !w2s || !ws) return MOE_ERR_INVALID_ARG;
   moe_workspace_layout_t L;
@@ -169,18 +174,29 @@ moe_status_t forward(const void* x, const float* logits, const uint8_t* w1, cons
   auto mark = [&]() { return ev ? cudaEventRecord(ev[evi++], s) : cudaSuccess; };
   MOE_CUDA_TRY(mark());
   moe::RouteArgs ra{logits, T, E, k, ids, tw, chunk_hist, L.nchunk, status, 1};
-  MOE_CUDA_TRY(moe::launch_route(ra, s));
-  MOE_CUDA_TRY(mark());
   moe::SortArgs sa{ids, T, E, k, chunk_hist, L.nchunk, counts, offsets, poff, mtb,
                    reinterpret_cast<int32_t*>(at(L.sorted_pair)), reinterpret_cast<int32_t*>(at(L.inv)),
                    inv_padded, status};
-  MOE_CUDA_TRY(moe::launch_scan(sa, s));
-  MOE_CUDA_TRY(mark());
-  MOE_CUDA_TRY(moe::launch_scatter(sa, s));
-  MOE_CUDA_TRY(mark());
+  if (T <= moe::kSmallRouteTokens) {
+    MOE_CUDA_TRY(moe::launch_route_sort_small(ra, sa, s));  // one launch for a decode step
+    MOE_CUDA_TRY(mark());
+  } else {
+    MOE_CUDA_TRY(moe::launch_route(ra, s));
+    MOE_CUDA_TRY(mark());
+    MOE_CUDA_TRY(moe::launch_scan(sa, s));
+    MOE_CUDA_TRY(mark());
+    MOE_CUDA_TRY(moe::launch_scatter(sa, s));
+    MOE_CUDA_TRY(mark());
+  }
   const int afmt = fmt == MOE_ACT_MXFP8 ? 0 : 1;
-  moe::QuantArgs qa{static_cast<const uint16_t*>(x), T, H, afmt, at(L.xq), at(L.xs), inv_padded, k};
-  MOE_CUDA_TRY(moe::launch_quant(qa, s));
+  if (x_scale == nullptr) {
+    moe::QuantArgs qa{static_cast<const uint16_t*>(x), T, H, afmt, at(L.xq), at(L.xs), inv_padded, k};
+    MOE_CUDA_TRY(moe::launch_quant(qa, s));
+  } else {
+    moe::PermuteArgs pa{static_cast<const uint8_t*>(x), x_scale, T, H, afmt == 0 ? (int64_t)H : (int64_t)H / 2,
+                        inv_padded, k, at(L.xq), at(L.xs)};
+    MOE_CUDA_TRY(moe::launch_permute_rows(pa, s));
+  }
   MOE_CUDA_TRY(mark());
 
   const int64_t mtiles_cap = L.rows_cap / kRowTile;
@@ -322,19 +338,46 @@ moe_status_t moe_quantize_mx(const void* x, int64_t rows, int K, moe_act_fmt_t f
 moe_status_t moe_a8w4_forward(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
                               const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I, int E, int k,
                               void* ws, size_t ws_bytes, void* stream) {
-  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP8, false);
+  return forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP8, false);
 }
 
 moe_status_t moe_a8w4_forward_prepacked(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
                                         const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I,
                                         int E, int k, void* ws, size_t ws_bytes, void* stream) {
-  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP8, true);
+  return forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP8, true);
 }
 
 moe_status_t moe_a4w4_forward_prepacked(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
                                         const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I,
                                         int E, int k, void* ws, size_t ws_bytes, void* stream) {
-  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP4, true);
+  return forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP4, true);
+}
+
+moe_status_t moe_forward_ex(const moe_forward_args_t* a) {
+  if (!a) return MOE_ERR_INVALID_ARG;
+  if (a->act_fmt != MOE_ACT_MXFP8 && a->act_fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (a->prequantized && a->T > 0 && !a->x_scale) return MOE_ERR_INVALID_ARG;
+  return forward(a->x, a->prequantized ? a->x_scale : nullptr, a->gate_logits, a->w1, a->w1_scale, a->w2,
+                 a->w2_scale, a->out, a->T, a->H, a->I, a->E, a->k, a->workspace, a->workspace_bytes, a->stream,
+                 a->act_fmt, a->weight_scales_prepacked != 0);
+}
+
+moe_status_t moe_a8w4_forward_prequant(const uint8_t* xq, const uint8_t* xq_scale, const float* logits,
+                                       const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s,
+                                       void* out, int64_t T, int H, int I, int E, int k, void* ws, size_t ws_bytes,
+                                       void* stream) {
+  if (T > 0 && !xq_scale) return MOE_ERR_INVALID_ARG;
+  return forward(xq, T > 0 ? xq_scale : nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes,
+                 stream, MOE_ACT_MXFP8, false);
+}
+
+moe_status_t moe_a4w4_forward_prequant(const uint8_t* xq, const uint8_t* xq_scale, const float* logits,
+                                       const uint8_t* w1, const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s,
+                                       void* out, int64_t T, int H, int I, int E, int k, void* ws, size_t ws_bytes,
+                                       void* stream) {
+  if (T > 0 && !xq_scale) return MOE_ERR_INVALID_ARG;
+  return forward(xq, T > 0 ? xq_scale : nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes,
+                 stream, MOE_ACT_MXFP4, false);
 }
 
 moe_status_t moe_prepack_scales(const uint8_t* scales, int64_t rows, int K, uint8_t* tiled, void* stream) {
@@ -352,7 +395,7 @@ moe_status_t moe_prepack_scales(const uint8_t* scales, int64_t rows, int K, uint
 moe_status_t moe_a4w4_forward(const void* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
                               const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H, int I, int E, int k,
                               void* ws, size_t ws_bytes, void* stream) {
-  return forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP4, false);
+  return forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, MOE_ACT_MXFP4, false);
 }
 
 moe_status_t moe_read_device_status(const void* ws, void* stream, moe_status_t* status_out) {
@@ -367,7 +410,7 @@ moe_status_t moe_read_device_status(const void* ws, void* stream, moe_status_t* 
   return MOE_OK;
 }
 
-int moe_forward_launch_count(int64_t T) { return T > 0 ? kForwardKernels : 0; }
+int moe_forward_launch_count(int64_t T) { return launch_count(T); }
 
 moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* logits, const uint8_t* w1,
                                  const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T,
@@ -380,17 +423,16 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* 
   for (int i = 0; i <= kForwardKernels && st == MOE_OK; ++i)
     if (cudaEventCreate(&ev[i]) != cudaSuccess) st = MOE_ERR_CUDA;
   if (st == MOE_OK)
-    st = forward(x, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt, prepacked_scales != 0,
-                 ev);
+    st = forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt,
+                 prepacked_scales != 0, ev);
+  const int nk = launch_count(T);
   if (st == MOE_OK && T > 0) {
-    if (cudaEventSynchronize(ev[kForwardKernels]) != cudaSuccess) st = MOE_ERR_CUDA;
-    for (int i = 0; i < kForwardKernels && st == MOE_OK; ++i) {
+    if (cudaEventSynchronize(ev[nk]) != cudaSuccess) st = MOE_ERR_CUDA;
+    for (int i = 0; i < nk && st == MOE_OK; ++i) {
       float ms = 0.0f;
       if (cudaEventElapsedTime(&ms, ev[i], ev[i + 1]) != cudaSuccess) st = MOE_ERR_CUDA;
       kernel_us[i] = ms * 1000.0f;
     }
-  } else if (st == MOE_OK) {
-    for (int i = 0; i < kForwardKernels; ++i) kernel_us[i] = 0.0f;
   }
   for (int i = 0; i <= kForwardKernels; ++i)
     if (ev[i]) cudaEventDestroy(ev[i]);

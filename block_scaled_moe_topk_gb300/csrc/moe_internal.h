@@ -56,6 +56,10 @@ cudaError_t launch_histogram(const SortArgs& a, cudaStream_t s);
 cudaError_t launch_scan(const SortArgs& a, cudaStream_t s);
 cudaError_t launch_scatter(const SortArgs& a, cudaStream_t s);
 cudaError_t launch_sort(const SortArgs& a, cudaStream_t s);
+// Batches of at most kSmallRouteTokens tokens: routing + sort (with padded outputs) in one
+// single-block kernel.
+constexpr int kSmallRouteTokens = 64;
+cudaError_t launch_route_sort_small(const RouteArgs& ra, const SortArgs& sa, cudaStream_t s);
 
 // quant.cu
 struct QuantArgs {
@@ -71,6 +75,20 @@ struct QuantArgs {
   int k;
 };
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
+// Prequantised activations [rows, code_bytes] + canonical scales [rows, K/32] -> padded expert
+// rows inv_padded[t*k + j] and the 128x4 tile layout (code_bytes % 16 == 0).
+struct PermuteArgs {
+  const uint8_t* codes_in;
+  const uint8_t* scales_in;
+  int64_t rows;
+  int K;
+  int64_t code_bytes;
+  const int32_t* inv_padded;
+  int k;
+  uint8_t* codes_out;
+  uint8_t* scales_out;
+};
+cudaError_t launch_permute_rows(const PermuteArgs& a, cudaStream_t s);
 // Canonical [rows, K/32] scales -> 128x4 tile layout (rows % 128 == 0, K % 128 == 0).
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst, cudaStream_t s);
 

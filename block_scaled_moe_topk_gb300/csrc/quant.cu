@@ -94,7 +94,37 @@ __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* src,
   }
 }
 
+// Prequantised input: token t's code row (and its scales) copied to its k padded expert rows,
+// scales into the 128x4 tile layout -- the quantiser's scatter without its arithmetic.
+__global__ void __launch_bounds__(256) permute_rows_kernel(PermuteArgs a) {
+  const int64_t row_bytes = a.code_bytes;        // multiple of 16
+  const int64_t chunks = row_bytes / 16;
+  const int64_t n = a.rows * chunks;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / chunks, c = i % chunks;
+    const uint4 v = *reinterpret_cast<const uint4*>(a.codes_in + t * row_bytes + c * 16);
+    for (int j = 0; j < a.k; ++j)
+      *reinterpret_cast<uint4*>(a.codes_out + (int64_t)a.inv_padded[t * a.k + j] * row_bytes + c * 16) = v;
+  }
+  const int nb = a.K / 32;
+  const int64_t ns = a.rows * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ns; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / nb;
+    const int kb = (int)(i % nb);
+    const uint8_t v = a.scales_in[t * nb + kb];
+    for (int j = 0; j < a.k; ++j) a.scales_out[sf_tile_offset(a.inv_padded[t * a.k + j], kb, a.K)] = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_permute_rows(const PermuteArgs& a, cudaStream_t s) {
+  const int64_t n = a.rows * (a.code_bytes / 16);
+  if (n == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
+  permute_rows_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst, cudaStream_t s) {
   const int64_t n = rows * (K / 128);

@@ -1,0 +1,88 @@
+// route_device.cuh -- top-k softmax gating of one token by one warp (shared by the routing
+// kernel and the fused small-batch route + sort kernel).
+//
+// "[HIP] gfx950 A8W4 fused_moe configs for DSv4.1 TP-sharded experts" (Changes: the top-k
+// softmax kernel): experts ranked by fp32 logit, descending, ties to the lower index; the k
+// selected softmax probabilities renormalised to sum 1, i.e. w_j = exp(l_j - l_max) /
+// sum_i exp(l_i - l_max) over the selected experts (the full softmax denominator cancels).
+#pragma once
+#include <cstdint>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Lane j < k of the calling warp receives slot j: expert id and renormalised weight.
+__device__ __forceinline__ void route_token(const float* l, int E, int k, int lane, int& id_out, float& w_out) {
+  constexpr int kMaxPerLane = kMaxExperts / 32;
+  const int per_lane = (E + 31) / 32;
+  float v[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (i < per_lane && e < E) ? l[e] : 0.0f;
+  }
+  uint32_t taken = 0;
+  int my_id = 0;
+  float my_val = 0.0f, lmax = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    // lane-local best among the experts not yet taken
+    float bv = 0.0f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (i < per_lane && e < E && !((taken >> i) & 1u)) {
+        if (bi == 0x7fffffff || route_better(v[i], e, bv, bi)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+    }
+    // warp arg-max (value desc, index asc)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || route_better(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi / 32);
+    if (j == 0) lmax = bv;
+    if (lane == j) {
+      my_id = bi;
+      my_val = bv;
+    }
+  }
+  // p_j = exp(l_j - l_max) without fp64 (scarce on this GPU): the difference is split
+  // exactly into s + e (two-sum), so its rounding is not amplified by exp, and
+  // exp(s + e) = expf(s) * (1 + e) because |e| <= ulp(s) / 2.
+  float p = 0.0f;
+  if (lane < k) {
+    const float sdiff = my_val - lmax;
+    const float bb = sdiff - my_val;
+    const float e = (my_val - (sdiff - bb)) + (-lmax - bb);
+    p = expf(sdiff) * (1.0f + e);
+  }
+  // z = sum of the k values as a compensated (hi, lo) pair, so w = p / z loses <= 1 ulp
+  float zh = p, zl = 0.0f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, zh, off);
+    const float ol = __shfl_xor_sync(0xffffffffu, zl, off);
+    const float sum = zh + oh;
+    const float bv = sum - zh;
+    zl += ol + ((zh - (sum - bv)) + (oh - bv));
+    zh = sum;
+  }
+  id_out = my_id;
+  w_out = __fdiv_rn(p, zh) * (1.0f - __fdiv_rn(zl, zh));
+}
+
+}  // namespace moe

@@ -12,6 +12,7 @@
 //   3. one warp per chunk walks its pairs in order and places each at
 //      offset[e] + chunk_base[e] + rank, so equal experts keep pair order.
 #include "moe_internal.h"
+#include "route_device.cuh"
 
 namespace moe {
 namespace {
@@ -133,7 +134,95 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
   }
 }
 
+// Small batches (T <= kSmallRouteTokens): routing, histogram, the prefix sums and the stable
+// scatter in one block, so a decode step pays one launch instead of three.  Same results as
+// route_kernel + scan_kernel + scatter_kernel.
+constexpr int kSmallMaxRows = kSmallRouteTokens * kMaxTopK;
+
+__global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArgs ra, SortArgs sa) {
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int next[kMaxExperts];
+  __shared__ int64_t off_s[kMaxExperts];
+  __shared__ int64_t poff_s[kMaxExperts];
+  __shared__ int ids_s[kSmallMaxRows];
+  __shared__ int64_t warp_tot[32];
+  __shared__ int64_t total;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int E = ra.E, k = ra.k;
+  const int64_t T = ra.T;
+  if (ra.reset_status && threadIdx.x < 8) ra.status[threadIdx.x] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    next[e] = 0;
+  }
+  __syncthreads();
+  for (int64_t t = warp; t < T; t += kScanThreads / 32) {
+    int id;
+    float w;
+    route_token(ra.logits + t * E, E, k, lane, id, w);
+    if (lane < k) {
+      ra.ids[t * k + lane] = id;
+      ra.w[t * k + lane] = w;
+      ids_s[t * k + lane] = id;
+      atomicAdd(&cnt[id], 1);
+    }
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int c = (e < E) ? cnt[e] : 0;
+  const int64_t off = block_exclusive_scan(c, warp_tot, &total);
+  const int64_t tot_rows = total;
+  const int64_t padded = ((int64_t)c + kRowTile - 1) / kRowTile * kRowTile;
+  const int64_t poff = block_exclusive_scan(padded, warp_tot, &total);
+  const int64_t tot_padded = total;
+  const int64_t toff = block_exclusive_scan(padded / kRowTile, warp_tot, &total);
+  const int64_t tot_tiles = total;
+  if (e < E) {
+    sa.counts[e] = c;
+    sa.offsets[e] = off;
+    sa.padded_offsets[e] = poff;
+    sa.mtile_base[e] = (int32_t)toff;
+    off_s[e] = off;
+    poff_s[e] = poff;
+  }
+  if (e == 0) {
+    sa.offsets[E] = tot_rows;
+    sa.padded_offsets[E] = tot_padded;
+    sa.mtile_base[E] = (int32_t)tot_tiles;
+  }
+  __syncthreads();
+  if (warp == 0) {  // stable scatter, pairs in ascending order
+    const int64_t R = T * k;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int64_t q0 = 0; q0 < R; q0 += 32) {
+      const int64_t q = q0 + lane;
+      const bool valid = q < R;
+      const int id = valid ? ids_s[q] : -1 - lane;
+      const uint32_t peers = __match_any_sync(0xffffffffu, id);
+      const int rank = __popc(peers & lt_mask);
+      const int leader = __ffs(peers) - 1;
+      const int base = valid ? next[id] : 0;
+      __syncwarp();
+      if (valid && lane == leader) next[id] = base + __popc(peers);
+      __syncwarp();
+      if (valid) {
+        const int64_t local = (int64_t)base + rank;
+        const int64_t r = off_s[id] + local;
+        sa.sorted_pair[r] = (int32_t)q;
+        sa.inv[q] = (int32_t)r;
+        sa.inv_padded[q] = (int32_t)(poff_s[id] + local);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_route_sort_small(const RouteArgs& ra, const SortArgs& sa, cudaStream_t s) {
+  if (ra.T == 0) return cudaSuccess;
+  route_sort_small_kernel<<<1, kScanThreads, 0, s>>>(ra, sa);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_scan(const SortArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;

@@ -253,6 +253,49 @@ moe_status_t moe_a4w4_forward_prepacked(const void* x_bf16, const float* gate_lo
                                         int E, int k, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The "prequant" forward ("add A4W4 and FP8 P2P transport support to MegaMoE", Test
+ * Plan: prequant end-to-end, i.e. without the activation quantisation): x arrives already
+ * quantised, as moe_quantize_mx writes it.
+ *   xq        A8W4: E4M3 codes [T, H]; A4W4: E2M1 codes [T, H/2]; 16-byte aligned
+ *   xq_scale  E8M0 [T, H/32] row-major
+ * Everything else as moe_a8w4_forward / moe_a4w4_forward (canonical weight scales).  The
+ * quantiser kernel is replaced by a copy of each token's codes to its k expert rows.
+ */
+moe_status_t moe_a8w4_forward_prequant(const uint8_t* xq, const uint8_t* xq_scale, const float* gate_logits,
+                                       const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
+                                       const uint8_t* w2_scale, void* out_bf16, int64_t T, int H, int I, int E,
+                                       int k, void* workspace, size_t workspace_bytes, void* stream);
+moe_status_t moe_a4w4_forward_prequant(const uint8_t* xq, const uint8_t* xq_scale, const float* gate_logits,
+                                       const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
+                                       const uint8_t* w2_scale, void* out_bf16, int64_t T, int H, int I, int E,
+                                       int k, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Every forward variant through one argument block: activation format, bf16 or
+ * prequantised input (x_scale then required), canonical or prepacked weight scales.
+ * Fields and rules as in the named entry points above.
+ */
+typedef struct {
+  moe_act_fmt_t act_fmt;
+  int prequantized;             /* 0: x is bf16 [T, H]; 1: x is codes, x_scale their E8M0 scales */
+  int weight_scales_prepacked;  /* 0: canonical [rows, K/32]; 1: moe_prepack_scales layout */
+  const void* x;
+  const uint8_t* x_scale;
+  const float* gate_logits;
+  const uint8_t* w1;
+  const uint8_t* w1_scale;
+  const uint8_t* w2;
+  const uint8_t* w2_scale;
+  void* out;
+  int64_t T;
+  int H, I, E, k;
+  void* workspace;
+  size_t workspace_bytes;
+  void* stream;
+} moe_forward_args_t;
+moe_status_t moe_forward_ex(const moe_forward_args_t* args);
+
+/*
  * Read the device status word a forward (or sort) left in `workspace`.
  * Synchronises `stream`, then copies 4 bytes to the host.  *status_out gets
  * MOE_OK or the moe_status_t a kernel recorded (MOE_ERR_DEVICE_TIMEOUT,
@@ -260,7 +303,8 @@ moe_status_t moe_a4w4_forward_prepacked(const void* x_bf16, const float* gate_lo
  */
 moe_status_t moe_read_device_status(const void* workspace, void* stream, moe_status_t* status_out);
 
-/* Number of kernels one forward call launches for T tokens (0 for T = 0). */
+/* Number of kernels one forward call launches for T tokens: 0 for T = 0, 5 for
+ * T <= 64 (routing and sort fused into one kernel), 7 above. */
 int moe_forward_launch_count(int64_t T);
 
 /*
@@ -270,7 +314,8 @@ int moe_forward_launch_count(int64_t T);
  * with a CUDA event recorded before the first kernel and after each kernel,
  * waits for the last event, and writes the duration of each kernel in
  * microseconds to kernel_us[moe_forward_launch_count(T)] (HOST array), in
- * launch order: route, scan, scatter, quant, gemm1, gemm2, combine.
+ * launch order: route, scan, scatter, quant, gemm1, gemm2, combine (T > 64) or
+ * route_sort, quant, gemm1, gemm2, combine (T <= 64).
  * Arguments and errors as for the forward; additionally synchronises on its
  * own events (so it is not graph-capturable) and creates/destroys them.
  */

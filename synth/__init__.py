@@ -11,6 +11,9 @@ Workload shapes follow the pages' layer shapes:
   * draft:        H=5120, I=1152, E=128, k=3  (DSpark draft experts, TP2 shard; same page)
   * pro:          H=7168, I=3072, E=384, k=6  (DeepSeek-V4-Pro; "add A4W4 and FP8 P2P transport
                   support to MegaMoE", Test Result: hidden/intermediate 7168/3072, experts/top-k 384/6)
+  * flash_tp2:    H=5120, I=1152, E=384, k=6  and
+  * draft_tp4:    H=5120, I=640,  E=128, k=3  -- the other two pairs of the tuned-shape grid
+                  (per-rank inter 640 / 1152 x experts 384x6 / 128x3) of the aiter page, Changes
 
 Sub-seeds, one per tensor: x = seed, logits = seed+1, expert bias = seed+2,
 W1 = seed+3, W2 = seed+4.
@@ -49,6 +52,8 @@ SHAPES = {
     "draft": Shape("draft", 5120, 1152, 128, 3, skew=True),
     "pro": Shape("pro", 7168, 3072, 384, 6),
     "pro_skew": Shape("pro_skew", 7168, 3072, 384, 6, skew=True),
+    "flash_tp2": Shape("flash_tp2", 5120, 1152, 384, 6),
+    "draft_tp4": Shape("draft_tp4", 5120, 640, 128, 3, skew=True),
 }
 
 TOKEN_SWEEPS = {

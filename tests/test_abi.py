@@ -99,4 +99,6 @@ def test_forward_validation_before_any_launch():
 
 def test_forward_launch_count():
     assert moe.moe_forward_launch_count(0) == 0
-    assert moe.moe_forward_launch_count(1) == 7
+    assert moe.moe_forward_launch_count(1) == 5
+    assert moe.moe_forward_launch_count(64) == 5
+    assert moe.moe_forward_launch_count(65) == 7

@@ -290,7 +290,7 @@ def test_profile_forward_matches_forward():
     moe.moe_a8w4_forward(x, lg, *W.dev, out_a, s.E, s.k, ws)
     us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws)
     torch.cuda.synchronize()
-    assert list(us) == list(moe.KERNEL_NAMES) and all(v > 0 for v in us.values())
+    assert list(us) == list(moe.KERNEL_NAMES_SMALL) and all(v > 0 for v in us.values())
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
 
 
@@ -338,3 +338,39 @@ def test_forward_api_limits_1024_experts_top8():
     want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, oracle.FMT_E4M3)
     rel, cos = compare(bits(out), want)
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+# --------------------------------------------------------------------------- prequant / forward_ex
+@pytest.mark.parametrize("shape,T,act", [("tiny", 16, moe.MOE_ACT_MXFP8), ("tiny", 16, moe.MOE_ACT_MXFP4),
+                                         ("flash_decode", 100, moe.MOE_ACT_MXFP8), ("pro", 512, moe.MOE_ACT_MXFP4)])
+def test_forward_prequant_and_ex_are_bit_identical(shape, T, act):
+    """Codes from moe_quantize_mx fed to the prequant forward give the bf16 forward's output bit
+    for bit; moe_forward_ex with prepacked weight scales does too."""
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 4).to(DEV), synth.gate_logits(T, s.E, 4).to(DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act), dtype=torch.uint8, device=DEV)
+    ref = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+    (moe.moe_a8w4_forward if act == moe.MOE_ACT_MXFP8 else moe.moe_a4w4_forward)(x, lg, *W.dev, ref, s.E, s.k, ws)
+    cb = s.H if act == moe.MOE_ACT_MXFP8 else s.H // 2
+    xq = torch.empty(T, cb, dtype=torch.uint8, device=DEV)
+    xs = torch.empty(T, s.H // 32, dtype=torch.uint8, device=DEV)
+    moe.moe_quantize_mx(x, act, xq, xs)
+    out = torch.empty_like(ref)
+    f = moe.moe_a8w4_forward_prequant if act == moe.MOE_ACT_MXFP8 else moe.moe_a4w4_forward_prequant
+    f(xq, xs, lg, *W.dev, out, s.E, s.k, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    w1, w1s, w2, w2s = W.dev
+    out2 = torch.empty_like(ref)
+    moe.moe_forward_ex(xq, lg, w1, _prepack(w1s), w2, _prepack(w2s), out2, s.E, s.k, ws, act_fmt=act, x_scale=xs,
+                       weight_scales_prepacked=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), ref.view(torch.int16))
+    assert moe.moe_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("shape,T", [("flash_tp2", 1), ("flash_tp2", 96), ("draft_tp4", 3), ("draft_tp4", 500)])
+def test_forward_tp_shard_shapes(shape, T):
+    """The remaining per-rank shapes of the tuned grid (inter 1152 at 384x6, inter 640 at 128x3)."""
+    _sampled_check(moe.MOE_ACT_MXFP8, synth.SHAPES[shape], T, 32)
