@@ -131,6 +131,35 @@ def layer_roofline(T, active, pk, E=SHAPE.E):
     return B, F, t_hbm, t_tc
 
 
+def shape_roofline(T, active, pk, H, I, E, k, fp4_act=False):
+    """Layer roofline for any shape: canonical bytes of the active experts plus x, logits, out;
+    6*T*k*H*I flops at the MXFP8 (2 x bf16) or MXFP4 (6 x bf16, the nominal ratios) peak."""
+    per_expert = 2 * I * H // 2 + 2 * I * H // 32 + H * I // 2 + H * I // 32
+    B = active * per_expert + T * H * 2 + T * E * 4 + T * H * 2
+    F = 6 * T * k * H * I
+    peak = (6.0 if fp4_act else 2.0) * pk["bf16"] * 1e12
+    return B, F, B / (pk["hbm"] * 1e9), F / peak
+
+
+def gemm_sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_scaled_moe_topk_gb300", "csrc")
+    for f in ("gemm.cu", "gemm_common.cuh", "ptx.cuh", "mx_device.cuh"):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """GEMM1 DRAM bytes per headline launch from the committed ncu summary, if it was taken
+    on the current GEMM sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    return d.get("bytes_per_headline_launch") if d.get("gemm_sources_sha256") == gemm_sources_sha() else None
+
+
 def gemm1_algorithmic(T, active):
     """GEMM1 bytes: active experts' W1 codes + scales, the routed activation rows and their
     scales read, the A2 rows and scales written; flops 2 * R * 2I * H."""
@@ -240,7 +269,8 @@ def run_ours(args):
     else:
         achieved, peak, unit, bound = g1_flops / g1_s / 1e12, 2.0 * pk["bf16"], "TFLOP/s", "tensor"
     roofline = {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": args.traffic, "kernel": "gemm1",
+                "frac": round(achieved / peak, 4),
+                "traffic": args.traffic if args.traffic is not None else measured_traffic(), "kernel": "gemm1",
                 "peak_source": pk["source"] + (" (MXFP8 = 2 x measured bf16)" if bound == "tensor" else ""),
                 "algorithmic_bytes": g1_bytes, "algorithmic_flops": g1_flops}
 
@@ -286,6 +316,67 @@ def run_ours(args):
                      "bytes": B, "flops": F, "bound": "hbm" if th >= tt else "tensor",
                      "roofline_us": round(max(th, tt) * 1e6, 2), "frac": round(max(th, tt) / (ms / 1e3), 4)})
         del g_
+
+    def point(f, weights, x_, lg_, E_, k_, H_, I_, ws_, fmt=moe.MOE_ACT_MXFP8):
+        o_ = torch.empty(x_.shape[0], H_, dtype=torch.bfloat16, device=dev)
+        f(x_, lg_, *weights, o_, E_, k_, ws_)
+        torch.cuda.synchronize()
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_):
+            f(x_, lg_, *weights, o_, E_, k_, ws_, stream=torch.cuda.current_stream())
+        ms_ = statistics.median(timed_replays(g_, 5, 3))
+        act_ = int((moe.workspace_views(ws_, x_.shape[0], H_, I_, E_, k_, fmt)["counts"] > 0).sum().item())
+        del g_
+        return ms_, act_
+
+    # ---------------------------------------------------------------- A4W4 (same weights)
+    a4 = []
+    if not args.quick_extras:
+        for t_ in (512, 1024, 8192):
+            xs_, lgs_ = make_workload(t_, rank, dev, E)
+            ms_, act_ = point(moe.moe_a4w4_forward_prepacked, W, xs_, lgs_, E, k, H, I, ws, moe.MOE_ACT_MXFP4)
+            B_, F_, th_, tt_ = shape_roofline(t_, act_, pk, H, I, E, k, fp4_act=True)
+            a4.append({"T": t_, "us": round(ms_ * 1e3, 2), "tok_s": round(t_ / (ms_ / 1e3), 1),
+                       "bound": "hbm" if th_ >= tt_ else "tensor", "roofline_us": round(max(th_, tt_) * 1e6, 2),
+                       "frac": round(max(th_, tt_) / (ms_ / 1e3), 4)})
+
+    # ---------------------------------------------------------------- prequant end to end (headline T)
+    xq_ = torch.empty(T, H, dtype=torch.uint8, device=dev)
+    xsc_ = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+    moe.moe_quantize_mx(x, moe.MOE_ACT_MXFP8, xq_, xsc_)
+
+    def prequant_fwd(x_, lg_, w1, w1s, w2, w2s, o_, E_, k_, ws_, stream=None):
+        moe.moe_forward_ex(xq_, lg_, w1, w1s, w2, w2s, o_, E_, k_, ws_, x_scale=xsc_, weight_scales_prepacked=True,
+                           stream=stream)
+    pre_ms, _ = point(prequant_fwd, W, x, lg, E, k, H, I, ws)
+
+    # ---------------------------------------------------------------- the other layer shapes of the configs
+    cfg = {}
+    if not args.quick_extras:
+        plans = [("flash_decode", [1, 2, 4, 8, 16, 32, 64]),
+                 ("draft", [2 ** i for i in range(16)] + [3072, 24576]),
+                 ("flash_tp2", [2 ** i for i in range(16)]),
+                 ("draft_tp4", [2 ** i for i in range(16)])]
+        for name, Ts in plans:
+            sh = synth.SHAPES[name]
+            Wsc = synth.weights_codes(sh.E, sh.H, sh.I, seed=0, device=dev)
+            t1, t2 = torch.empty_like(Wsc[1]), torch.empty_like(Wsc[3])
+            moe.moe_prepack_scales(Wsc[1], t1)
+            moe.moe_prepack_scales(Wsc[3], t2)
+            Wsh = (Wsc[0], t1, Wsc[2], t2)
+            ws_sh = torch.empty(max(moe.moe_workspace_bytes(t_, sh.H, sh.I, sh.E, sh.k) for t_ in Ts),
+                                dtype=torch.uint8, device=dev)
+            rows_sh = []
+            for t_ in Ts:
+                xs_ = synth.x_bf16(t_, sh.H, seed=rank, device=dev)
+                lgs_ = synth.gate_logits(t_, sh.E, seed=rank, skew=sh.skew, device=dev)
+                ms_, act_ = point(fwd, Wsh, xs_, lgs_, sh.E, sh.k, sh.H, sh.I, ws_sh)
+                B_, F_, th_, tt_ = shape_roofline(t_, act_, pk, sh.H, sh.I, sh.E, sh.k)
+                rows_sh.append({"T": t_, "us": round(ms_ * 1e3, 2), "active_experts": act_,
+                                "frac": round(max(th_, tt_) / (ms_ / 1e3), 4)})
+            cfg[f"{name} H={sh.H} I={sh.I} E={sh.E} k={sh.k}{' skewed' if sh.skew else ''}"] = rows_sh
+            del Wsc, Wsh, t1, t2, ws_sh
+            torch.cuda.empty_cache()
     clk = clocks.stop()
 
     # ---------------------------------------------------------------- CPU oracle baseline
@@ -308,6 +399,8 @@ def run_ours(args):
                    "parallelism": f"dp{world} (independent token batches, no collective)"},
         "us_per_call": round(ms_per_step * 1e3, 2), "routed_rows_s": round(value * k, 1),
         "canonical_scales_us_per_call": round(canon_ms * 1e3, 2),
+        "prequant_us_per_call": round(pre_ms * 1e3, 2),
+        "a4w4": a4, "config_sweeps": cfg,
         "layer_roofline": {"bytes": B, "flops": F, "active_experts": active, "t_hbm_us": round(th * 1e6, 2),
                            "t_tensor_us": round(tt * 1e6, 2), "bound": "hbm" if th >= tt else "tensor",
                            "frac": round(max(th, tt) / (ms_per_step / 1e3), 4), "peaks": pk["source"]},
@@ -387,6 +480,7 @@ def main():
     ap.add_argument("--experts", type=int, default=SHAPE.E,
                     help="expert count (smaller values only for profiler captures of a small case)")
     ap.add_argument("--quick", action="store_true", help="only W+K plain forwards, no report (profiling)")
+    ap.add_argument("--quick-extras", action="store_true", help="skip the A4W4 and per-config sweeps")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=64)
