@@ -14,26 +14,26 @@
 //   warp 10     producer: with canonical weight scales, 4-byte cp.async copies that rearrange
 //               them into that layout; with prepacked scales, the TMA of the weight tile and
 //               the bulk copies of its scales (so the two halves of a stage issue in parallel);
-//   warp 1      TMEM owner and MMA issuer (one thread): tcgen05.cp of the scales to TMEM, then
+//   warp 1      TMEM owner; its lane 0 issues tcgen05.cp of the scales to TMEM, then
 //               tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1, scale_vec 1X) or kind::mxf4 (E2M1 x E2M1,
-//               scale_vec 2X) into a 128x256 fp32 accumulator in TMEM;
+//               scale_vec 2X) into a 128x256 fp32 accumulator in TMEM, from precomputed
+//               descriptors (the issuing thread's instruction stream bounds the stage rate);
 //   warps 2..9  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one routed row) per
 //               thread; warps 2-5 take columns [0, 128), warps 6-9 columns [128, 256).  Each
 //               thread pulls its 128 columns into registers, releases TMEM at once, and only
 //               then runs the SwiGLU / requant / store work, so that work overlaps the next
-//               tile's MMAs.
+//               tile's MMAs.  GEMM2 rows leave through shared memory as TMA stores.
 // A 4-deep shared-memory ring with full/empty mbarriers overlaps the weight stream with the
 // MMAs; each tile's canonical weight-scale block is prefetched into L2 at the tile start.
-// The producer loop is short on purpose (its per-stage issue cost, not DRAM latency, set the
-// pace of an earlier version): barrier probes are inlined, addressing is hoisted per tile.  Every wait is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
-// status word, lets its own copies and MMAs drain (again bounded), frees TMEM and returns.
+// The experts' M-tile prefix is staged in shared memory for the per-tile lookups.  Every wait
+// is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the status word, lets its
+// own copies and MMAs drain (again bounded), frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <mutex>
 
 #include "gemm_common.cuh"
-#include "mx_device.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -50,7 +50,12 @@ constexpr int kSfaOff = kABytes + kBBytes;
 constexpr int kSfbOff = kSfaOff + 1024;
 constexpr int kStageBytes = kSfbOff + 2048;  // 51 KiB, a multiple of 1024
 constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers/flags + alignment slack
+constexpr int kTileBaseOff = kBarOff + 256;       // M-tile prefix over experts, int32 [E+1]
+// GEMM2 epilogue staging: one 32-row x 32-column bf16 block (2 KiB) per epilogue warp
+constexpr int kOutStageOff = (kTileBaseOff + 4 * (kMaxExperts + 1) + 1023) / 1024 * 1024;
+constexpr int kOutStageBytes = 32 * 32 * 2;
+constexpr int kSmemBytes = kOutStageOff + kEpiWarps * kOutStageBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "single-CTA GEMM shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;   // accumulator uses columns [0, 256)
 constexpr uint32_t kSfSlotCols = 32;
@@ -58,11 +63,11 @@ constexpr uint32_t kSfSlotCols = 32;
 struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_act;
   CUtensorMap tmap_w;
+  CUtensorMap tmap_out;   // GEMM2: y2 bf16 [rows_cap, N], box 32 columns x 32 rows, 64-byte swizzle
   const uint8_t* act_sf;
   const uint8_t* w_sf;    // canonical [E, N, K/32], or the 128x4 tile layout when w_sf_tiled
   const int32_t* counts;
-  const int64_t* padded_offsets;
-  const int32_t* mtile_base;
+  const int32_t* mtile_base;  // expert e's rows start at row 128 * mtile_base[e]
   uint8_t* out_codes;
   uint8_t* out_sf;
   uint16_t* out_bf16;
@@ -72,33 +77,6 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   int w_sf_tiled;
   int test_stall;
 };
-
-template <int ACT>
-struct ActTraits;
-template <>
-struct ActTraits<0> {                  // E4M3 activations x E2M1 weights
-  static constexpr int kKPerStage = 128;
-  static constexpr int kMmaK = 32;
-  // The weight tile lands with an 8-byte gap after every 8 bytes of codes (32 KiB of shared
-  // memory) but its transaction count is the 16 KiB of packed codes read from global memory.
-  static constexpr int kBTxBytes = kNTile * 64;
-  static constexpr uint32_t kIdescFmt = (0u << 7) | (5u << 10);
-};
-template <>
-struct ActTraits<1> {                  // E2M1 x E2M1, packed
-  static constexpr int kKPerStage = 256;
-  static constexpr int kMmaK = 64;
-  static constexpr int kBTxBytes = kNTile * 128;
-  static constexpr uint32_t kIdescFmt = (1u << 7) | (1u << 10);
-};
-
-// Block-scaled instruction descriptor: formats, N>>3 at [17,23), E8M0 scales (bit 23),
-// M>>4 at [24,29); K-major A and B; scale-factor byte ids at [29,31) (A) and [4,6) (B).
-template <int ACT>
-__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
-  return ActTraits<ACT>::kIdescFmt | ((uint32_t)(kNTile >> 3) << 17) | (1u << 23) |
-         ((uint32_t)(kRowTile >> 4) << 24) | (sf_id << 29) | (sf_id << 4);
-}
 
 template <int ACT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -118,8 +96,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const uint32_t drain_bar = tmem_full_bar + 16;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * (2 * kStages + 3));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int32_t* tile_base = reinterpret_cast<int32_t*>(smem + kTileBaseOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // the per-tile expert lookup (a binary search) reads shared memory, not global memory: it
+  // sits on the producer's path at every tile boundary
+  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) tile_base[e] = p.mtile_base[e];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       // canonical scales: warp 0's expect_tx arrive + 32 cp.async arrivals of the scale warp;
@@ -146,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const int NT = p.N / kNTile;
   const int K = p.K;
   const int nks = (K + TR::kKPerStage - 1) / TR::kKPerStage;
-  const int64_t total_tiles = (int64_t)p.mtile_base[p.E] * NT;
+  const int64_t total_tiles = (int64_t)tile_base[p.E] * NT;
 
   if (warp == 0 || warp == kScaleWarp) {
     // ------------------------------------------------------------------ producers
@@ -161,8 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
     bool ok = !p.test_stall;  // the test hook leaves every stage unfilled
     for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      const Tile tc = decode_tile(tile, p.mtile_base, p.E, NT);
-      const int64_t row0 = p.padded_offsets[tc.e] + (int64_t)tc.mt * kRowTile;
+      const Tile tc = decode_tile(tile, tile_base, p.E, NT);
+      const int64_t row0 = ((int64_t)tile_base[tc.e] + tc.mt) * kRowTile;
       const int n0 = tc.nt * kNTile;
       const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
       const int64_t sf_row32 = (int64_t)32 * (K / 32);        // 32 weight rows of scales
@@ -230,82 +212,91 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       for (int s = 0; s < kStages; ++s)
         if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull, true);
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    int slot = 0;
-    uint32_t phase = 0, acc_phase = 0;
-    bool ok = true, issued = false;
-    for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      if (!warp_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      for (int ks = 0; ks < nks; ++ks) {
-        if (!warp_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
+    // ------------------------------------------------------------------ MMA issuer (lane 0)
+    // tcgen05.cp / tcgen05.mma / tcgen05.commit are single-thread instructions: the loop runs
+    // on one lane with its descriptors precomputed, so the issuing thread's own instruction
+    // stream stays short between stages.
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      // descriptors of slot 0; a slot adds kStageBytes, an MMA step 32 bytes (start address
+      // field, in 16-byte units; shared-memory offsets stay below 2^18, so no carry)
+      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(sbase + kABytes, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t sfa_desc0 = smem_desc(sbase + kSfaOff, 128, 128, kLayoutNone);
+      const uint64_t sfb_desc0 = smem_desc(sbase + kSfbOff, 128, 128, kLayoutNone);
+      constexpr uint64_t kSlotStep = kStageBytes >> 4;
+      constexpr uint32_t kHalfStep = (kAtomsPerStage * 512) >> 4;  // second 128 weight rows
+      const bool gathered = !p.w_sf_tiled;
+      for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        if (!lane_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int kvalid = min(TR::kKPerStage, K - ks * TR::kKPerStage);
-        const int katoms = kvalid / 128;
-        const int nmma = kvalid / TR::kMmaK;
-        if (lane == 0) {
-          fence_proxy_async_smem();  // scales written by cp.async, read by tcgen05.cp
-          const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!lane_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (gathered) fence_proxy_async_smem();  // scales written by cp.async, read by tcgen05.cp
+          const uint64_t so = (uint64_t)slot * kSlotStep;
           const uint32_t sf_col = tmem_base + kSfCol0 + (uint32_t)slot * kSfSlotCols;
-          for (int ka = 0; ka < katoms; ++ka) {
-            tc_cp_32x128b_warpx4(sf_col + ka * 4, smem_desc(st + kSfaOff + ka * 512, 128, 128, kLayoutNone));
+          const int kvalid = min(TR::kKPerStage, K - ks * TR::kKPerStage);
+          const int katoms = kvalid == TR::kKPerStage ? kAtomsPerStage : kvalid / 128;
+          const int nmma = kvalid == TR::kKPerStage ? kMmaPerStage : kvalid / TR::kMmaK;
 #pragma unroll
-            for (int na = 0; na < 2; ++na)
-              tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8 + na * 4,
-                                   smem_desc(st + kSfbOff + na * (kAtomsPerStage * 512) + ka * 512, 128, 128,
-                                             kLayoutNone));
+          for (int ka = 0; ka < kAtomsPerStage; ++ka) {
+            if (ka < katoms) {
+              tc_cp_32x128b_warpx4(sf_col + ka * 4, sfa_desc0 + so + ka * 32);
+              tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8, sfb_desc0 + so + ka * 32);
+              tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8 + 4, sfb_desc0 + so + kHalfStep + ka * 32);
+            }
           }
 #pragma unroll
           for (int j = 0; j < kMmaPerStage; ++j) {
             if (j < nmma) {
-              const uint64_t adesc = smem_desc(st + j * 32, 16, 1024, kLayoutSwizzle128B);
-              const uint64_t bdesc = smem_desc(st + kABytes + j * 32, 16, 1024, kLayoutSwizzle128B);
-              const int kblk = j * TR::kMmaK / 32;  // first 32-block of this MMA inside the stage
-              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3));
-              const uint32_t sfa = sf_col + (kblk >> 2) * 4;
-              const uint32_t sfb = sf_col + kSfaCols + (kblk >> 2) * 8;
+              const int kblk = j * (TR::kMmaK / 32);  // first 32-block of this MMA inside the stage
+              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3), kRowTile);
               const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
-              if (ACT == 0) tc_mma_mxf8f6f4(tmem_base, adesc, bdesc, idesc, sfa, sfb, acc);
-              else tc_mma_mxf4(tmem_base, adesc, bdesc, idesc, sfa, sfb, acc);
+              if (ACT == 0)
+                tc_mma_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
+                                sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * 8, acc);
+              else
+                tc_mma_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, sf_col + (kblk >> 2) * 4,
+                            sf_col + kSfaCols + (kblk >> 2) * 8, acc);
             }
           }
           tc_commit(empty_bar(slot));
           issued = true;
+          if (++slot == kStages) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
-        __syncwarp();
-        if (++slot == kStages) {
-          slot = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
+        tc_commit(tmem_full_bar);
+        acc_phase ^= 1u;
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(tmem_full_bar);
-      __syncwarp();
-      acc_phase ^= 1u;
+      // Make sure no MMA or TMEM copy of this CTA is still running before TMEM is freed.
+      if (issued) {
+        tc_commit(drain_bar);
+        lane_wait(drain_bar, 0, sync, 100000000ull, true);
+      }
     }
-    // Make sure no MMA or TMEM copy of this CTA is still running before TMEM is freed.
-    issued = __shfl_sync(0xffffffffu, issued, 0);
-    if (issued) {
-      if (lane == 0) tc_commit(drain_bar);
-      __syncwarp();
-      warp_wait(drain_bar, 0, sync, 100000000ull, true);
-    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue
     const int quad = warp & 3;         // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // accumulator columns [half*128, half*128 + 128)
     uint32_t acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile tc = decode_tile(tile, p.mtile_base, p.E, NT);
+      const Tile tc = decode_tile(tile, tile_base, p.E, NT);
       const int row_local = tc.mt * kRowTile + quad * 32 + lane;
       const bool valid = row_local < p.counts[tc.e];
-      const int64_t prow = p.padded_offsets[tc.e] + row_local;
+      const int64_t prow = (int64_t)tile_base[tc.e] * kRowTile + row_local;
       if (!warp_wait(tmem_full_bar, acc_phase, sync, p.timeout_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
@@ -318,49 +309,45 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty_bar);
       acc_phase ^= 1u;
-      if (EPI == 0) {
-        const int I = p.N / 2;
+      if (EPI == 1 && __all_sync(0xffffffffu, valid)) {
+        // GEMM2 rows as bf16 (round to nearest even) through shared memory when all 32 rows of
+        // this warp are routed rows: each 32-column chunk leaves as one TMA store.  (Every lane
+        // storing 16-byte pieces of its own row kept the load/store pipe so busy that the MMA
+        // warp's barrier polls queued behind the stores: GEMM2 ran 25 % slower at large T.)
+        // A warp with padding rows stores its valid rows directly (few such warps at large T;
+        // at small T most rows are padding, and skipping them saves HBM writes).
+        const uint32_t buf = sbase + kOutStageOff + (uint32_t)(warp - 2) * kOutStageBytes;
+        const int x0 = tc.nt * kNTile + half * 128;
+        const int y0 = (tile_base[tc.e] + tc.mt) * kRowTile + quad * 32;
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-byte swizzle: 16-byte chunk ^= (row/2)%4
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = silu_mul(acc[2 * i], acc[2 * i + 1]);  // h in place
+        for (int c = 0; c < 4; ++c) {
+          if (lane == 0) bulk_wait_read_all();  // the previous store has read the buffer
+          __syncwarp();
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          const float* h = acc + 32 * blk;
-          float amax = 0.0f;
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-          const MxScale sc = mx_scale<ACT>(amax);
-          const int kb = tc.nt * 4 + half * 2 + blk;  // 32-wide block of h
-          if (valid) {
-            if (ACT == 0) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out_codes + prow * I + kb * 32);
-              const uint2 c0 = pack_e4m3x8(h, sc.mult), c1 = pack_e4m3x8(h + 8, sc.mult);
-              const uint2 c2 = pack_e4m3x8(h + 16, sc.mult), c3 = pack_e4m3x8(h + 24, sc.mult);
-              dst[0] = make_uint4(c0.x, c0.y, c1.x, c1.y);
-              dst[1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(p.out_codes + prow * (I / 2) + kb * 16);
-              *dst = make_uint4(pack_e2m1x8(h, sc.mult), pack_e2m1x8(h + 8, sc.mult), pack_e2m1x8(h + 16, sc.mult),
-                                pack_e2m1x8(h + 24, sc.mult));
+            for (int q = 0; q < 4; ++q) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(acc[32 * c + 8 * i + 2 * q], acc[32 * c + 8 * i + 2 * q + 1]);
+              w[q] = *reinterpret_cast<const uint32_t*>(&b);
             }
-            p.out_sf[sf_tile_offset(prow, kb, I)] = sc.byte;
+            st_shared_v4(buf + (uint32_t)lane * 64u + (((uint32_t)i ^ swz) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmap_out, buf, x0 + 32 * c, y0);
+            bulk_commit_group();
           }
         }
-      } else if (valid) {
-        // GEMM2 rows stored as bf16 (round to nearest even); the combine accumulates in fp32
-        uint4* d4 = reinterpret_cast<uint4*>(p.out_bf16 + prow * p.N + tc.nt * kNTile + half * 128);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          uint32_t w[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * i + 2 * c], acc[8 * i + 2 * c + 1]);
-            w[c] = *reinterpret_cast<const uint32_t*>(&b);
-          }
-          d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+      } else {
+        store_acc_rows<ACT, EPI>(acc, valid, prow, tc.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16);
       }
     }
   }
+
+  if (EPI == 1 && warp >= 2 && warp < 2 + kEpiWarps && lane == 0) bulk_wait_all();  // y2 stores done
 
   tc_fence_before();
   __syncthreads();
@@ -416,12 +403,21 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
     }
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  if (EPI == 1) {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.rows_cap};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.N * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&p.tmap_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_bf16, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   p.act_sf = a.act_sf;
   p.w_sf = a.w_sf;
   p.w_sf_tiled = a.w_sf_tiled;
   p.test_stall = a.test_stall;
   p.counts = a.counts;
-  p.padded_offsets = a.padded_offsets;
   p.mtile_base = a.mtile_base;
   p.out_codes = a.out_codes;
   p.out_sf = a.out_sf;

@@ -1,18 +1,49 @@
-// gemm_common.cuh -- pieces shared by the grouped GEMM kernels (gemm.cu, gemm_swap.cu):
-// tile decoding over the experts' M tiles, bounded mbarrier waits, SwiGLU, and the driver
-// entry point that encodes TMA tensor maps.
+// gemm_common.cuh -- pieces shared by the grouped GEMM kernels (gemm.cu: one CTA per tile,
+// gemm_pair.cu: CTA pairs): operand-format traits and the instruction descriptor, tile
+// decoding over the experts' M tiles, bounded mbarrier waits, the epilogue stores (SwiGLU +
+// MX requant, or bf16 rows), and the driver entry point that encodes TMA tensor maps.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "moe_internal.h"
+#include "mx_device.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
+
+template <int ACT>
+struct ActTraits;
+template <>
+struct ActTraits<0> {                  // E4M3 activations x E2M1 weights
+  static constexpr int kKPerStage = 128;
+  static constexpr int kMmaK = 32;
+  // The weight tile lands with an 8-byte gap after every 8 bytes of codes (32 KiB of shared
+  // memory) but its transaction count is the 16 KiB of packed codes read from global memory.
+  static constexpr int kBTxBytes = kNTile * 64;
+  static constexpr uint32_t kIdescFmt = (0u << 7) | (5u << 10);
+};
+template <>
+struct ActTraits<1> {                  // E2M1 x E2M1, packed
+  static constexpr int kKPerStage = 256;
+  static constexpr int kMmaK = 64;
+  static constexpr int kBTxBytes = kNTile * 128;
+  static constexpr uint32_t kIdescFmt = (1u << 7) | (1u << 10);
+};
+
+// Block-scaled instruction descriptor: formats, N>>3 at [17,23), E8M0 scales (bit 23),
+// M>>4 at [24,29) (M = 128 for one CTA, 256 for a CTA pair); K-major A and B; scale-factor
+// byte ids at [29,31) (A) and [4,6) (B).
+template <int ACT>
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id, int M) {
+  return ActTraits<ACT>::kIdescFmt | ((uint32_t)(kNTile >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+         (sf_id << 29) | (sf_id << 4);
+}
 
 struct Tile {
   int e, mt, nt;
@@ -91,7 +122,65 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const S
   return __all_sync(0xffffffffu, ok);
 }
 
+// Single-thread form for roles that run on one lane (TMA and MMA issue): no vote.
+__device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity, const Sync& s, uint64_t limit_ns,
+                                          bool drain = false) {
+  return mbar_try_wait(bar, parity) || bounded_wait(bar, parity, s, limit_ns, drain);
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdiv_rn(g, 1.0f + expf(-g)) * u; }
+
+// Epilogue of one thread: `acc` holds accumulator columns [half*128, half*128 + 128) of N tile
+// nt for routed row prow (nothing is stored unless `valid`).
+//   EPI 0 (GEMM1): h_j = silu(gate_j) * up_j over the 64 interleaved (gate, up) column pairs,
+//                  then MX requantisation of h: two 32-wide blocks, E4M3 (ACT 0) or E2M1
+//                  (ACT 1) codes into out_codes [rows, N/2 or N/4] and one E8M0 byte per block
+//                  into out_sf (128x4 tile layout over N/2 columns).
+//   EPI 1 (GEMM2): the fp32 row rounded to bf16 (nearest even) into out_bf16 [rows, N].
+template <int ACT, int EPI>
+__device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, int64_t prow, int nt, int half, int N,
+                                               uint8_t* out_codes, uint8_t* out_sf, uint16_t* out_bf16) {
+  if (EPI == 0) {
+    const int I = N / 2;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] = silu_mul(acc[2 * i], acc[2 * i + 1]);  // h in place
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const float* h = acc + 32 * blk;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+      const MxScale sc = mx_scale<ACT>(amax);
+      const int kb = nt * 4 + half * 2 + blk;  // 32-wide block of h
+      if (valid) {
+        if (ACT == 0) {
+          uint4* dst = reinterpret_cast<uint4*>(out_codes + prow * I + kb * 32);
+          const uint2 c0 = pack_e4m3x8(h, sc.mult), c1 = pack_e4m3x8(h + 8, sc.mult);
+          const uint2 c2 = pack_e4m3x8(h + 16, sc.mult), c3 = pack_e4m3x8(h + 24, sc.mult);
+          dst[0] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+          dst[1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(out_codes + prow * (I / 2) + kb * 16);
+          *dst = make_uint4(pack_e2m1x8(h, sc.mult), pack_e2m1x8(h + 8, sc.mult), pack_e2m1x8(h + 16, sc.mult),
+                            pack_e2m1x8(h + 24, sc.mult));
+        }
+        out_sf[sf_tile_offset(prow, kb, I)] = sc.byte;
+      }
+    }
+  } else if (valid) {
+    uint4* d4 = reinterpret_cast<uint4*>(out_bf16 + prow * N + nt * kNTile + half * 128);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint32_t w[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * i + 2 * c], acc[8 * i + 2 * c + 1]);
+        w[c] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

@@ -104,8 +104,7 @@ struct GemmArgs {
   int w_sf_tiled;
   int E, N, K;
   const int32_t* counts;
-  const int64_t* padded_offsets;
-  const int32_t* mtile_base;
+  const int32_t* mtile_base;  // [E+1]; expert e's padded rows start at 128 * mtile_base[e]
   int64_t max_tiles;      // host upper bound on tiles (grid sizing)
   uint8_t* out_codes;     // GEMM1: A2 codes [rows_cap, N/2 or N/4]
   uint8_t* out_sf;        // GEMM1: A2 scales, 128x4 tile layout over N/2 columns
@@ -115,7 +114,10 @@ struct GemmArgs {
   int num_sms;
   int test_stall;         // test hook: the producer issues nothing, so the MMA warp's wait expires
 };
+// gemm.cu: one CTA per 128-row x 256-column tile (any weight-scale layout).
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+// gemm_pair.cu: CTA pairs, 256-row x 256-column tiles (prepacked weight scales only).
+cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t s);
 
 
 // combine.cu

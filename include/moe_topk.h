@@ -84,6 +84,24 @@ typedef enum {
   MOE_ACT_MXFP4 = 1  /* E2M1 activation codes, two per byte (A4W4)         */
 } moe_act_fmt_t;
 
+/*
+ * How the grouped GEMMs tile the routed rows (moe_forward_ex, moe_profile_forward).
+ *   MOE_GEMM_TILES_SINGLE  one CTA per 128-row x 256-column tile (any weight-scale layout);
+ *   MOE_GEMM_TILES_PAIR    a cluster of two CTAs per 256-row x 256-column tile, one
+ *                          tcgen05.mma.cta_group::2 for both SMs: half the weight bytes per SM
+ *                          and a deeper copy ring, but the same tensor-pipe work per SM per
+ *                          stage, and an expert with an odd number of 128-row tiles pays for
+ *                          a whole pair.  Needs prepacked weight scales.
+ *   MOE_GEMM_TILES_AUTO    single tiles (the faster form on every shape measured so far,
+ *                          T = 1 ... 32768); every other entry point uses this rule.
+ * The two forms compute the same rows with the same arithmetic (results are bit-identical).
+ */
+typedef enum {
+  MOE_GEMM_TILES_AUTO = 0,
+  MOE_GEMM_TILES_SINGLE = 1,
+  MOE_GEMM_TILES_PAIR = 2
+} moe_gemm_tiles_t;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(moe_status_t status);
 
@@ -292,6 +310,8 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   void* stream;
+  int gemm_tiles;               /* moe_gemm_tiles_t; MOE_GEMM_TILES_PAIR without prepacked
+                                   weight scales is MOE_ERR_INVALID_ARG */
 } moe_forward_args_t;
 moe_status_t moe_forward_ex(const moe_forward_args_t* args);
 
@@ -310,7 +330,8 @@ int moe_forward_launch_count(int64_t T);
 /*
  * Profiling form of the forward: enqueues exactly the launch sequence of
  * moe_a8w4_forward (fmt = MOE_ACT_MXFP8) or moe_a4w4_forward (MOE_ACT_MXFP4),
- * or of their *_prepacked forms when prepacked_scales != 0,
+ * or of their *_prepacked forms when prepacked_scales != 0, with the GEMM
+ * tiling gemm_tiles (moe_gemm_tiles_t, as in moe_forward_ex),
  * with a CUDA event recorded before the first kernel and after each kernel,
  * waits for the last event, and writes the duration of each kernel in
  * microseconds to kernel_us[moe_forward_launch_count(T)] (HOST array), in
@@ -323,7 +344,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x_bf16, const fl
                                  const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
                                  const uint8_t* w2_scale, void* out_bf16, int64_t T, int H, int I, int E,
                                  int k, void* workspace, size_t workspace_bytes, void* stream,
-                                 int prepacked_scales, float* kernel_us);
+                                 int prepacked_scales, int gemm_tiles, float* kernel_us);
 
 #ifdef __cplusplus
 }

@@ -126,6 +126,8 @@ def _check_intermediates(act, x, lg, W, E, k, ws, tokens=None):
     e_of_q = ids_h.reshape(-1)
     assert np.array_equal(inv_p, poff[e_of_q] + (i - o[e_of_q]))
     assert np.all(np.diff(poff) % 128 == 0) and np.all(np.diff(poff) >= c)
+    # the GEMMs locate an expert's rows from its M-tile prefix: padded offset = 128 * tiles before it
+    assert np.array_equal(poff, 128 * v["mtile_base"].cpu().numpy().astype(np.int64))
     # quantised activations: every routed row of a (sampled) token equals the oracle's row
     toks = np.arange(T) if tokens is None else np.asarray(tokens)
     want_c, want_s = oracle.quantize_rows_bf16(synth.bf16_bits(x)[toks], act)
@@ -368,6 +370,35 @@ def test_forward_prequant_and_ex_are_bit_identical(shape, T, act):
     torch.cuda.synchronize()
     assert torch.equal(out2.view(torch.int16), ref.view(torch.int16))
     assert moe.moe_read_device_status(ws) == 0
+
+
+# --------------------------------------------------------------------------- CTA-pair tiles
+@pytest.mark.parametrize("shape,T,act", [("tiny", 16, moe.MOE_ACT_MXFP8), ("tiny", 16, moe.MOE_ACT_MXFP4),
+                                         ("flash_decode", 300, moe.MOE_ACT_MXFP8), ("draft", 3072, moe.MOE_ACT_MXFP8),
+                                         ("draft_tp4", 2000, moe.MOE_ACT_MXFP4), ("pro", 1024, moe.MOE_ACT_MXFP4),
+                                         ("pro", 4096, moe.MOE_ACT_MXFP8)])
+def test_forward_pair_tiles_are_bit_identical(shape, T, act):
+    """256-row tiles on CTA pairs (tcgen05 cta_group::2) give the single-CTA tiles' output bit for
+    bit: both GEMMs, experts with odd and even tile counts (odd ones leave the second CTA of
+    their last pair without rows), and A4W4's ragged last K stage (I = 640)."""
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 6).to(DEV), synth.gate_logits(T, s.E, 6, skew=s.skew).to(DEV)
+    w1, w1s, w2, w2s = W.dev
+    Wp = (w1, _prepack(w1s), w2, _prepack(w2s))
+    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act), dtype=torch.uint8, device=DEV)
+    outs = []
+    for tiles in (moe.MOE_GEMM_TILES_SINGLE, moe.MOE_GEMM_TILES_PAIR):
+        out = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+        moe.moe_forward_ex(x, lg, *Wp, out, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=True, gemm_tiles=tiles)
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(ws) == 0
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    if shape == "tiny":
+        want = oracle.moe_forward(synth.bf16_bits(x.cpu()), lg.cpu().numpy(), *W.host, s.E, s.k, act)
+        rel, cos = compare(bits(outs[1]), want)
+        assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
 
 
 @pytest.mark.parametrize("shape,T", [("flash_tp2", 1), ("flash_tp2", 96), ("draft_tp4", 3), ("draft_tp4", 500)])
