@@ -131,7 +131,7 @@ __device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity, const S
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdiv_rn(g, 1.0f + expf(-g)) * u; }
 
 // Epilogue of one thread: `acc` holds accumulator columns [half*128, half*128 + 128) of N tile
-// nt for routed row prow (nothing is stored unless `valid`).
+// nt for routed row prow (nothing is stored unless `valid`).  Called by all 32 lanes of a warp.
 //   EPI 0 (GEMM1): h_j = silu(gate_j) * up_j over the 64 interleaved (gate, up) column pairs,
 //                  then MX requantisation of h: two 32-wide blocks, E4M3 (ACT 0) or E2M1
 //                  (ACT 1) codes into out_codes [rows, N/2 or N/4] and one E8M0 byte per block
@@ -142,6 +142,15 @@ __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, in
                                                uint8_t* out_codes, uint8_t* out_sf, uint16_t* out_bf16) {
   if (EPI == 0) {
     const int I = N / 2;
+    // Padding rows of an expert's segment hold whatever the workspace held before: their
+    // accumulators can be huge or non-finite, which sends the IEEE division in silu_mul down
+    // its slow path for the whole warp (measured: A4W4 GEMM1 1.5 -> 2.2 ms with stale bytes).
+    // Skip warps with no routed row; give padding lanes of the others zeros.
+    if (!__any_sync(0xffffffffu, valid)) return;
+    if (!valid) {
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+    }
 #pragma unroll
     for (int i = 0; i < 64; ++i) acc[i] = silu_mul(acc[2 * i], acc[2 * i + 1]);  // h in place
 #pragma unroll

@@ -372,6 +372,34 @@ def test_forward_prequant_and_ex_are_bit_identical(shape, T, act):
     assert moe.moe_read_device_status(ws) == 0
 
 
+def test_forward_independent_of_stale_workspace():
+    """The padding rows of the expert segments are never written: a workspace full of stale
+    random bytes gives the zeroed workspace's output bit for bit (both formats, both tilings)."""
+    s = synth.SHAPES["flash_decode"]
+    W = _weights(s)
+    T = 300
+    x, lg = synth.x_bf16(T, s.H, 8).to(DEV), synth.gate_logits(T, s.E, 8).to(DEV)
+    w1, w1s, w2, w2s = W.dev
+    Wp = (w1, _prepack(w1s), w2, _prepack(w2s))
+    gen = torch.Generator(device=DEV).manual_seed(8)
+    for act in (moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4):
+        nbytes = moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act)
+        outs = []
+        for fill in ("zeros", "random"):
+            for tiles in (moe.MOE_GEMM_TILES_SINGLE, moe.MOE_GEMM_TILES_PAIR):
+                ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+                if fill == "random":
+                    ws.random_(0, 256, generator=gen)
+                out = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+                moe.moe_forward_ex(x, lg, *Wp, out, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=True,
+                                   gemm_tiles=tiles)
+                torch.cuda.synchronize()
+                assert moe.moe_read_device_status(ws) == 0
+                outs.append(out)
+        for o in outs[1:]:
+            assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
 # --------------------------------------------------------------------------- CTA-pair tiles
 @pytest.mark.parametrize("shape,T,act", [("tiny", 16, moe.MOE_ACT_MXFP8), ("tiny", 16, moe.MOE_ACT_MXFP4),
                                          ("flash_decode", 300, moe.MOE_ACT_MXFP8), ("draft", 3072, moe.MOE_ACT_MXFP8),
