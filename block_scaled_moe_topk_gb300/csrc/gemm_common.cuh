@@ -128,7 +128,10 @@ __device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity, const S
   return mbar_try_wait(bar, parity) || bounded_wait(bar, parity, s, limit_ns, drain);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return __fdiv_rn(g, 1.0f + expf(-g)) * u; }
+// h = silu(g) * u = g / (1 + exp(-g)) * u in fp32 with the fast exponential and reciprocal
+// (a few ulp; the 128 per-thread evaluations share the SM with the MMA-issuing thread).  Large
+// negative g: exp(-g) = inf, g / inf = -0, the limit.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 // Epilogue of one thread: `acc` holds accumulator columns [half*128, half*128 + 128) of N tile
 // nt for routed row prow (nothing is stored unless `valid`).  Called by all 32 lanes of a warp.
@@ -143,8 +146,8 @@ __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, in
   if (EPI == 0) {
     const int I = N / 2;
     // Padding rows of an expert's segment hold whatever the workspace held before: their
-    // accumulators can be huge or non-finite, which sends the IEEE division in silu_mul down
-    // its slow path for the whole warp (measured: A4W4 GEMM1 1.5 -> 2.2 ms with stale bytes).
+    // accumulators can be huge or non-finite, which sent an IEEE division in SwiGLU down its
+    // slow path for the whole warp (measured: A4W4 GEMM1 1.5 -> 2.2 ms with stale bytes).
     // Skip warps with no routed row; give padding lanes of the others zeros.
     if (!__any_sync(0xffffffffu, valid)) return;
     if (!valid) {

@@ -2,8 +2,8 @@
 // per 1x32 block ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical
 // Details; OCP Microscaling v1.0 scale rule s = floor(log2 amax) - emax + 127).
 //
-// Each thread owns 8 consecutive elements (one 16-byte load); four threads form a
-// 32-element block and agree on its amax with two shuffles.  In the forward the
+// Each thread owns 16 consecutive elements (two 16-byte loads); two threads form a
+// 32-element block and agree on its amax with one shuffle.  In the forward the
 // codes of token t are written straight to its k padded expert rows
 // inv_padded[t*k + j] (the permute is fused here), and the scales go to the
 // 128x4 tile layout that the GEMM's tensor-memory scale copy reads.
@@ -20,60 +20,68 @@ namespace moe {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kColsPerBlock = kQuantThreads * 8;
 
+// Thread i of the grid owns elements [16c, 16c + 16) of row r, (r, c) = (i / (K/16), i % (K/16));
+// lanes 2m and 2m+1 hold one 32-element block (K % 32 == 0 keeps the pairs inside a row) and
+// agree on its amax with one shuffle.  Every lane of a warp runs the same number of rounds.
 template <int FMT>
 __global__ void __launch_bounds__(kQuantThreads) quant_kernel(QuantArgs a) {
   const int K = a.K;
-  const int col_blocks = (K + kColsPerBlock - 1) / kColsPerBlock;
-  const int64_t work = a.rows * col_blocks;
-  for (int64_t wi = blockIdx.x; wi < work; wi += gridDim.x) {
-    const int64_t row = wi / col_blocks;
-    const int col0 = (int)(wi % col_blocks) * kColsPerBlock + threadIdx.x * 8;
-    const bool active = col0 < K;
-    float v[8];
+  const int chunks = K / 16;
+  const int64_t n = a.rows * chunks;
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < n; base += stride) {
+    const int64_t i = base + lane;
+    const bool active = i < n;
+    const int64_t row = active ? i / chunks : 0;
+    const int col0 = active ? (int)(i % chunks) * 16 : 0;
+    float v[16];
     if (active) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(a.x + row * K + col0);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + row * K + col0);
+      const uint4 r0 = src[0], r1 = src[1];
+      const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      for (int q = 0; q < 8; ++q) {
+        v[2 * q] = __uint_as_float(w[q] << 16);
+        v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      for (int q = 0; q < 16; ++q) v[q] = 0.0f;
     }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    if (!active) continue;  // whole 4-lane groups are active or not (K % 32 == 0)
+    if (!active) continue;  // both lanes of a pair are active or not (n is even)
     const MxScale sc = mx_scale<FMT>(amax);
     const int kb = col0 / 32;
-    const bool scale_writer = (threadIdx.x & 3) == 0;
+    const bool scale_writer = (col0 & 31) == 0;
     if (FMT == 0) {
-      const uint2 codes = pack_e4m3x8(v, sc.mult);
-      if (a.inv_padded == nullptr) {
-        *reinterpret_cast<uint2*>(a.codes + row * K + col0) = codes;
+      const uint2 c0 = pack_e4m3x8(v, sc.mult), c1 = pack_e4m3x8(v + 8, sc.mult);
+      if (a.inv_padded == nullptr) {  // caller's buffers: 8-byte alignment is what the API asks
+        uint2* dst = reinterpret_cast<uint2*>(a.codes + row * K + col0);
+        dst[0] = c0;
+        dst[1] = c1;
         if (scale_writer) a.scales[row * (K / 32) + kb] = sc.byte;
-      } else {
+      } else {  // workspace rows (256-byte aligned, K % 32 == 0): one 16-byte store per row
+        const uint4 c = make_uint4(c0.x, c0.y, c1.x, c1.y);
         for (int j = 0; j < a.k; ++j) {
           const int64_t prow = a.inv_padded[row * a.k + j];
-          *reinterpret_cast<uint2*>(a.codes + prow * K + col0) = codes;
+          *reinterpret_cast<uint4*>(a.codes + prow * K + col0) = c;
           if (scale_writer) a.scales[sf_tile_offset(prow, kb, K)] = sc.byte;
         }
       }
     } else {
-      const uint32_t codes = pack_e2m1x8(v, sc.mult);
+      const uint2 c = make_uint2(pack_e2m1x8(v, sc.mult), pack_e2m1x8(v + 8, sc.mult));
       if (a.inv_padded == nullptr) {
-        *reinterpret_cast<uint32_t*>(a.codes + row * (K / 2) + col0 / 2) = codes;
+        *reinterpret_cast<uint2*>(a.codes + row * (K / 2) + col0 / 2) = c;
         if (scale_writer) a.scales[row * (K / 32) + kb] = sc.byte;
       } else {
         for (int j = 0; j < a.k; ++j) {
           const int64_t prow = a.inv_padded[row * a.k + j];
-          *reinterpret_cast<uint32_t*>(a.codes + prow * (K / 2) + col0 / 2) = codes;
+          *reinterpret_cast<uint2*>(a.codes + prow * (K / 2) + col0 / 2) = c;
           if (scale_writer) a.scales[sf_tile_offset(prow, kb, K)] = sc.byte;
         }
       }
@@ -135,10 +143,9 @@ cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8
 }
 
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
-  const int col_blocks = (a.K + kColsPerBlock - 1) / kColsPerBlock;
-  const int64_t work = a.rows * col_blocks;
-  if (work == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)std::min<int64_t>(work, 152 * 16);
+  const int64_t n = a.rows * (a.K / 16);
+  if (n == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<int64_t>((n + kQuantThreads - 1) / kQuantThreads, 152 * 8);
   if (a.fmt == 0) quant_kernel<0><<<grid, kQuantThreads, 0, s>>>(a);
   else quant_kernel<1><<<grid, kQuantThreads, 0, s>>>(a);
   return cudaGetLastError();
