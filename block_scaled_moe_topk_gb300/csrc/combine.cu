@@ -22,17 +22,31 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < work; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / groups;
     const int c0 = (int)(i % groups) * 8;
+    // all k row loads in flight before the first FMA (k <= kMaxTopK)
+    int rows[kMaxTopK];
+    float w[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) {
+        rows[j] = a.inv_padded[t * k + j];
+        w[j] = a.w[t * k + j];
+      }
+    uint4 raw[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) raw[j] = *reinterpret_cast<const uint4*>(a.y2 + (int64_t)rows[j] * H + c0);
     float acc[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const float w = a.w[t * k + j];
-      const uint4 raw = *reinterpret_cast<const uint4*>(a.y2 + (int64_t)a.inv_padded[t * k + j] * H + c0);
-      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc[2 * c] = fmaf(w, __uint_as_float(u[c] << 16), acc[2 * c]);              // low half: column c0+2c
-        acc[2 * c + 1] = fmaf(w, __uint_as_float(u[c] & 0xFFFF0000u), acc[2 * c + 1]);
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {  // slot order
+        const uint32_t u[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          acc[2 * c] = fmaf(w[j], __uint_as_float(u[c] << 16), acc[2 * c]);              // low half: column c0+2c
+          acc[2 * c + 1] = fmaf(w[j], __uint_as_float(u[c] & 0xFFFF0000u), acc[2 * c + 1]);
+        }
       }
     }
     uint32_t packed[4];

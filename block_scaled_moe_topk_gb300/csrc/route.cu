@@ -16,6 +16,7 @@ constexpr int kRouteWarps = 8;
 
 // Block b routes tokens [b*kTokensPerChunk, (b+1)*kTokensPerChunk) and, if asked,
 // writes the chunk's expert histogram to chunk_hist[e * nchunk + b].
+template <int kPerLane>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   __shared__ int hist[kMaxExperts];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -30,7 +31,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   for (int64_t t = t_begin + warp; t < t_end; t += kRouteWarps) {
     int my_id;
     float my_w;
-    route_token(a.logits + t * E, E, k, lane, my_id, my_w);
+    route_token<kPerLane>(a.logits + t * E, E, k, lane, my_id, my_w);
     if (lane < k) {
       a.ids[t * k + lane] = my_id;
       a.w[t * k + lane] = my_w;
@@ -66,7 +67,8 @@ __global__ void __launch_bounds__(256) histogram_kernel(SortArgs a) {
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   const int64_t blocks = (a.T + kTokensPerChunk - 1) / kTokensPerChunk;
   if (blocks == 0) return cudaSuccess;
-  route_kernel<<<(unsigned)blocks, kRouteWarps * 32, 0, s>>>(a);
+  if (a.E <= 512) route_kernel<16><<<(unsigned)blocks, kRouteWarps * 32, 0, s>>>(a);
+  else route_kernel<32><<<(unsigned)blocks, kRouteWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -17,8 +17,10 @@ __device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib)
 }
 
 // Lane j < k of the calling warp receives slot j: expert id and renormalised weight.
+// kMaxPerLane >= ceil(E / 32): logits held per lane (fewer registers for smaller E).
+template <int kMaxPerLane = kMaxExperts / 32>
 __device__ __forceinline__ void route_token(const float* l, int E, int k, int lane, int& id_out, float& w_out) {
-  constexpr int kMaxPerLane = kMaxExperts / 32;
+  static_assert(kMaxPerLane <= 32, "taken-mask width");
   const int per_lane = (E + 31) / 32;
   float v[kMaxPerLane];
 #pragma unroll

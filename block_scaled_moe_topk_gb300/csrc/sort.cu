@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
 // route_kernel + scan_kernel + scatter_kernel.
 constexpr int kSmallMaxRows = kSmallRouteTokens * kMaxTopK;
 
+template <int kPerLane>
 __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArgs ra, SortArgs sa) {
   __shared__ int cnt[kMaxExperts];
   __shared__ int next[kMaxExperts];
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArg
   for (int64_t t = warp; t < T; t += kScanThreads / 32) {
     int id;
     float w;
-    route_token(ra.logits + t * E, E, k, lane, id, w);
+    route_token<kPerLane>(ra.logits + t * E, E, k, lane, id, w);
     if (lane < k) {
       ra.ids[t * k + lane] = id;
       ra.w[t * k + lane] = w;
@@ -220,7 +221,8 @@ __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArg
 
 cudaError_t launch_route_sort_small(const RouteArgs& ra, const SortArgs& sa, cudaStream_t s) {
   if (ra.T == 0) return cudaSuccess;
-  route_sort_small_kernel<<<1, kScanThreads, 0, s>>>(ra, sa);
+  if (ra.E <= 512) route_sort_small_kernel<16><<<1, kScanThreads, 0, s>>>(ra, sa);
+  else route_sort_small_kernel<32><<<1, kScanThreads, 0, s>>>(ra, sa);
   return cudaGetLastError();
 }
 
