@@ -40,28 +40,45 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kThreads = 352;    // TMA producer, MMA, 8 epilogue warps, weight-scale copier
 constexpr int kEpiWarps = 8;
 constexpr int kScaleWarp = 10;
-constexpr int kABytes = kRowTile * 128;   // 128 rows x 128 bytes
-constexpr int kBBytes = kNTile * 128;     // 256 rows x 128 bytes (shared-memory footprint)
-constexpr int kSfaOff = kABytes + kBBytes;
-constexpr int kSfbOff = kSfaOff + 1024;
-constexpr int kStageBytes = kSfbOff + 2048;  // 51 KiB, a multiple of 1024
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kTileBaseOff = kBarOff + 256;       // M-tile prefix over experts, int32 [E+1]
-// GEMM2 epilogue staging: one 32-row x 32-column bf16 block (2 KiB) per epilogue warp
-constexpr int kOutStageOff = (kTileBaseOff + 4 * (kMaxExperts + 1) + 1023) / 1024 * 1024;
-constexpr int kOutStageBytes = 32 * 32 * 2;
-constexpr int kSmemBytes = kOutStageOff + kEpiWarps * kOutStageBytes + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "single-CTA GEMM shared memory");
+constexpr int kOutStageBytes = 32 * 32 * 2;  // GEMM2 epilogue staging: 32 rows x 32 bf16 per warp
+
+// Shared-memory geometry of one CTA.  Regular tiles stage all 128 activation rows of a tile
+// per K stage.  The small-batch form (every tile has at most 16 routed rows: T <= 16, since a
+// token routes to an expert at most once) stages 16 rows, which leaves room for 6 stages of
+// the weight stream instead of 4 (the MMA still reads 128 rows: rows 16..127 come from the
+// following bytes of the stage and only reach accumulator rows that are never stored).
+template <int ACT, bool SMALLA>
+struct Geo {
+  static constexpr int kARows = SMALLA ? 16 : kRowTile;
+  static constexpr int kABytes = kARows * 128;             // activation slot
+  static constexpr int kBOff = kABytes;                    // weight tile, 1024-aligned (SW128)
+  static constexpr int kBBytes = kNTile * 128;             // 256 rows x 128 bytes of shared memory
+  static constexpr int kSfaOff = kBOff + kBBytes;
+  static constexpr int kSfaBytes = ActTraits<ACT>::kKPerStage / 128 * 512;
+  static constexpr int kSfbOff = kSfaOff + kSfaBytes;      // two 128-row halves of kSfaBytes each
+  static constexpr int kStageBytes = (kSfbOff + 2 * kSfaBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = SMALLA ? (ACT == 0 ? 6 : 5) : 4;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kTileBaseOff = kBarOff + 256;      // M-tile prefix over experts, int32 [E+1]
+  static constexpr bool kOutStaging = !SMALLA;            // GEMM2 rows leave as TMA stores
+  static constexpr int kOutStageOff = (kTileBaseOff + 4 * (kMaxExperts + 1) + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes =
+      (kOutStaging ? kOutStageOff + kEpiWarps * kOutStageBytes : kTileBaseOff + 4 * (kMaxExperts + 1)) +
+      1024;  // + alignment slack
+  static_assert(kBOff % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+  static_assert(kSmemBytes <= 232448, "single-CTA GEMM shared memory");
+  static_assert(kStages * 32 <= 256, "TMEM scale slots");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;   // accumulator uses columns [0, 256)
 constexpr uint32_t kSfSlotCols = 32;
 
 struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_act;
+  CUtensorMap tmap_act16;  // the same activation codes, box 128 B x 16 rows (small-batch form)
   CUtensorMap tmap_w;
   CUtensorMap tmap_out;   // GEMM2: y2 bf16 [rows_cap, N], box 32 columns x 32 rows, 64-byte swizzle
   const uint8_t* act_sf;
@@ -78,9 +95,14 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   int test_stall;
 };
 
-template <int ACT, int EPI>
+template <int ACT, int EPI, bool SMALLA>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using TR = ActTraits<ACT>;
+  using G = Geo<ACT, SMALLA>;
+  constexpr int kStages = G::kStages;
+  constexpr int kStageBytes = G::kStageBytes;
+  constexpr int kSfaOff = G::kSfaOff;
+  constexpr int kSfbOff = G::kSfbOff;
   constexpr int kMmaPerStage = TR::kKPerStage / TR::kMmaK;  // 4
   constexpr int kAtomsPerStage = TR::kKPerStage / 128;      // k-atoms of 4 scale blocks
   constexpr uint32_t kSfaCols = kAtomsPerStage * 4;
@@ -88,15 +110,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + kBarOff;
+  const uint32_t bar0 = sbase + G::kBarOff;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   const uint32_t tmem_full_bar = bar0 + 8u * (2 * kStages);
   const uint32_t tmem_empty_bar = tmem_full_bar + 8;
   const uint32_t drain_bar = tmem_full_bar + 16;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * (2 * kStages + 3));
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + G::kBarOff + 8 * (2 * kStages + 3));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int32_t* tile_base = reinterpret_cast<int32_t*>(smem + kTileBaseOff);
+  int32_t* tile_base = reinterpret_cast<int32_t*>(smem + G::kTileBaseOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // the per-tile expert lookup (a binary search) reads shared memory, not global memory: it
@@ -166,16 +188,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           if (tma_warp) {
             // activation side, plus the weight codes when the scale warp is busy gathering
             mbar_arrive_expect_tx(full_bar(slot),
-                                  (uint32_t)(kABytes + katoms * 512 + (p.w_sf_tiled ? 0 : TR::kBTxBytes)));
-            tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
+                                  (uint32_t)(G::kABytes + katoms * 512 + (p.w_sf_tiled ? 0 : TR::kBTxBytes)));
+            tma_load_2d(st, SMALLA ? &p.tmap_act16 : &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
             bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
                       (uint32_t)katoms * 512u, full_bar(slot));
-            if (!p.w_sf_tiled) tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
+            if (!p.w_sf_tiled) tma_load_3d(st + G::kBOff, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
           } else if (p.w_sf_tiled) {
             // weight side with prepacked scales: codes + one contiguous run of k-atoms per
             // 128-row half of the tile, issued in parallel with warp 0
             mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(TR::kBTxBytes + 2 * katoms * 512));
-            tma_load_3d(st + kABytes, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
+            tma_load_3d(st + G::kBOff, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
 #pragma unroll
             for (int na = 0; na < 2; ++na)
               bulk_load(st + kSfbOff + na * (kAtomsPerStage * 512),
@@ -223,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       // descriptors of slot 0; a slot adds kStageBytes, an MMA step 32 bytes (start address
       // field, in 16-byte units; shared-memory offsets stay below 2^18, so no carry)
       const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kLayoutSwizzle128B);
-      const uint64_t b_desc0 = smem_desc(sbase + kABytes, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(sbase + G::kBOff, 16, 1024, kLayoutSwizzle128B);
       const uint64_t sfa_desc0 = smem_desc(sbase + kSfaOff, 128, 128, kLayoutNone);
       const uint64_t sfb_desc0 = smem_desc(sbase + kSfbOff, 128, 128, kLayoutNone);
       constexpr uint64_t kSlotStep = kStageBytes >> 4;
@@ -309,14 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty_bar);
       acc_phase ^= 1u;
-      if (EPI == 1 && __all_sync(0xffffffffu, valid)) {
+      if (EPI == 1 && G::kOutStaging && __all_sync(0xffffffffu, valid)) {
         // GEMM2 rows as bf16 (round to nearest even) through shared memory when all 32 rows of
         // this warp are routed rows: each 32-column chunk leaves as one TMA store.  (Every lane
         // storing 16-byte pieces of its own row kept the load/store pipe so busy that the MMA
         // warp's barrier polls queued behind the stores: GEMM2 ran 25 % slower at large T.)
         // A warp with padding rows stores its valid rows directly (few such warps at large T;
         // at small T most rows are padding, and skipping them saves HBM writes).
-        const uint32_t buf = sbase + kOutStageOff + (uint32_t)(warp - 2) * kOutStageBytes;
+        const uint32_t buf = sbase + G::kOutStageOff + (uint32_t)(warp - 2) * kOutStageBytes;
         const int x0 = tc.nt * kNTile + half * 128;
         const int y0 = (tile_base[tc.e] + tc.mt) * kRowTile + quad * 32;
         const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-byte swizzle: 16-byte chunk ^= (row/2)%4
@@ -347,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     }
   }
 
-  if (EPI == 1 && warp >= 2 && warp < 2 + kEpiWarps && lane == 0) bulk_wait_all();  // y2 stores done
+  if (EPI == 1 && G::kOutStaging && warp >= 2 && warp < 2 + kEpiWarps && lane == 0) bulk_wait_all();  // y2 stores
 
   tc_fence_before();
   __syncthreads();
@@ -356,14 +378,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------- host side
-template <int ACT, int EPI>
+template <int ACT, int EPI, bool SMALLA>
 cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
+  using G = Geo<ACT, SMALLA>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<ACT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    err = cudaFuncSetAttribute(moe_gemm_kernel<ACT, EPI, SMALLA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               G::kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
@@ -381,6 +405,11 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
     const cuuint32_t es[2] = {1, 1};
     if (encode(&p.tmap_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.act), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const cuuint32_t box16[2] = {128, 16};
+    if (encode(&p.tmap_act16, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.act), dims, strides, box16,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -429,15 +458,19 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   p.K = a.K;
   const int64_t grid = std::min<int64_t>(a.num_sms, a.max_tiles);
   if (grid <= 0) return cudaSuccess;
-  moe_gemm_kernel<ACT, EPI><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p);
+  moe_gemm_kernel<ACT, EPI, SMALLA><<<(unsigned)grid, kThreads, G::kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0>(a, s) : launch_typed<0, 1>(a, s);
-  return a.epilogue == 0 ? launch_typed<1, 0>(a, s) : launch_typed<1, 1>(a, s);
+  if (a.small_a) {
+    if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, true>(a, s) : launch_typed<0, 1, true>(a, s);
+    return a.epilogue == 0 ? launch_typed<1, 0, true>(a, s) : launch_typed<1, 1, true>(a, s);
+  }
+  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, false>(a, s) : launch_typed<0, 1, false>(a, s);
+  return a.epilogue == 0 ? launch_typed<1, 0, false>(a, s) : launch_typed<1, 1, false>(a, s);
 }
 
 }  // namespace moe
