@@ -46,24 +46,24 @@ constexpr int kScaleWarp = 10;
 constexpr int kOutStageBytes = 32 * 32 * 2;  // GEMM2 epilogue staging: 32 rows x 32 bf16 per warp
 
 // Shared-memory geometry of one CTA.  Regular tiles stage all 128 activation rows of a tile
-// per K stage.  The small-batch form (every tile has at most 16 routed rows: T <= 16, since a
-// token routes to an expert at most once) stages 16 rows, which leaves room for 6 stages of
-// the weight stream instead of 4 (the MMA still reads 128 rows: rows 16..127 come from the
-// following bytes of the stage and only reach accumulator rows that are never stored).
-template <int ACT, bool SMALLA>
+// per K stage.  Small batches stage fewer -- AROWS = 16 when T <= 16, 64 when T <= 64 (no
+// tile then has more routed rows: a token routes to an expert at most once) -- which leaves
+// room for more stages of the latency-bound weight stream.  The MMA still reads 128 rows:
+// rows past AROWS come from the following bytes of the stage and only reach accumulator rows
+// that are never stored.
+template <int ACT, int AROWS>
 struct Geo {
-  static constexpr int kARows = SMALLA ? 16 : kRowTile;
-  static constexpr int kABytes = kARows * 128;             // activation slot
+  static constexpr int kABytes = AROWS * 128;              // activation slot
   static constexpr int kBOff = kABytes;                    // weight tile, 1024-aligned (SW128)
   static constexpr int kBBytes = kNTile * 128;             // 256 rows x 128 bytes of shared memory
   static constexpr int kSfaOff = kBOff + kBBytes;
   static constexpr int kSfaBytes = ActTraits<ACT>::kKPerStage / 128 * 512;
   static constexpr int kSfbOff = kSfaOff + kSfaBytes;      // two 128-row halves of kSfaBytes each
   static constexpr int kStageBytes = (kSfbOff + 2 * kSfaBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = SMALLA ? (ACT == 0 ? 6 : 5) : 4;
+  static constexpr int kStages = AROWS == kRowTile ? 4 : (AROWS == 16 && ACT == 0 ? 6 : 5);
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kTileBaseOff = kBarOff + 256;      // M-tile prefix over experts, int32 [E+1]
-  static constexpr bool kOutStaging = !SMALLA;            // GEMM2 rows leave as TMA stores
+  static constexpr bool kOutStaging = AROWS == kRowTile;  // GEMM2 rows leave as TMA stores
   static constexpr int kOutStageOff = (kTileBaseOff + 4 * (kMaxExperts + 1) + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes =
       (kOutStaging ? kOutStageOff + kEpiWarps * kOutStageBytes : kTileBaseOff + 4 * (kMaxExperts + 1)) +
@@ -77,8 +77,7 @@ constexpr uint32_t kSfCol0 = 256;   // accumulator uses columns [0, 256)
 constexpr uint32_t kSfSlotCols = 32;
 
 struct GemmParams {  // 64-byte aligned through its CUtensorMap members
-  CUtensorMap tmap_act;
-  CUtensorMap tmap_act16;  // the same activation codes, box 128 B x 16 rows (small-batch form)
+  CUtensorMap tmap_act;   // activation codes, box 128 B x AROWS rows
   CUtensorMap tmap_w;
   CUtensorMap tmap_out;   // GEMM2: y2 bf16 [rows_cap, N], box 32 columns x 32 rows, 64-byte swizzle
   const uint8_t* act_sf;
@@ -95,10 +94,10 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   int test_stall;
 };
 
-template <int ACT, int EPI, bool SMALLA>
+template <int ACT, int EPI, int AROWS>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using TR = ActTraits<ACT>;
-  using G = Geo<ACT, SMALLA>;
+  using G = Geo<ACT, AROWS>;
   constexpr int kStages = G::kStages;
   constexpr int kStageBytes = G::kStageBytes;
   constexpr int kSfaOff = G::kSfaOff;
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             // activation side, plus the weight codes when the scale warp is busy gathering
             mbar_arrive_expect_tx(full_bar(slot),
                                   (uint32_t)(G::kABytes + katoms * 512 + (p.w_sf_tiled ? 0 : TR::kBTxBytes)));
-            tma_load_2d(st, SMALLA ? &p.tmap_act16 : &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
+            tma_load_2d(st, &p.tmap_act, full_bar(slot), ks * 128, (int)row0);
             bulk_load(st + kSfaOff, p.act_sf + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
                       (uint32_t)katoms * 512u, full_bar(slot));
             if (!p.w_sf_tiled) tma_load_3d(st + G::kBOff, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
@@ -378,15 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------- host side
-template <int ACT, int EPI, bool SMALLA>
+template <int ACT, int EPI, int AROWS>
 cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
-  using G = Geo<ACT, SMALLA>;
+  using G = Geo<ACT, AROWS>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<ACT, EPI, SMALLA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(moe_gemm_kernel<ACT, EPI, AROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                G::kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
@@ -401,15 +400,10 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   {
     const cuuint64_t dims[2] = {act_row_bytes, (cuuint64_t)a.rows_cap};
     const cuuint64_t strides[1] = {act_row_bytes};
-    const cuuint32_t box[2] = {128, (cuuint32_t)kRowTile};
+    const cuuint32_t box[2] = {128, (cuuint32_t)AROWS};
     const cuuint32_t es[2] = {1, 1};
     if (encode(&p.tmap_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.act), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-    const cuuint32_t box16[2] = {128, 16};
-    if (encode(&p.tmap_act16, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.act), dims, strides, box16,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -458,19 +452,23 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   p.K = a.K;
   const int64_t grid = std::min<int64_t>(a.num_sms, a.max_tiles);
   if (grid <= 0) return cudaSuccess;
-  moe_gemm_kernel<ACT, EPI, SMALLA><<<(unsigned)grid, kThreads, G::kSmemBytes, s>>>(p);
+  moe_gemm_kernel<ACT, EPI, AROWS><<<(unsigned)grid, kThreads, G::kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  if (a.small_a) {
-    if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, true>(a, s) : launch_typed<0, 1, true>(a, s);
-    return a.epilogue == 0 ? launch_typed<1, 0, true>(a, s) : launch_typed<1, 1, true>(a, s);
+  // small batches (at most a_rows routed rows in any tile) stage fewer activation rows; A4W4's
+  // larger stages gain no extra stage from a 64-row slot
+  if (a.a_rows <= 16) {
+    if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, 16>(a, s) : launch_typed<0, 1, 16>(a, s);
+    return a.epilogue == 0 ? launch_typed<1, 0, 16>(a, s) : launch_typed<1, 1, 16>(a, s);
   }
-  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, false>(a, s) : launch_typed<0, 1, false>(a, s);
-  return a.epilogue == 0 ? launch_typed<1, 0, false>(a, s) : launch_typed<1, 1, false>(a, s);
+  if (a.a_rows <= 64 && a.act_fmt == 0)
+    return a.epilogue == 0 ? launch_typed<0, 0, 64>(a, s) : launch_typed<0, 1, 64>(a, s);
+  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, kRowTile>(a, s) : launch_typed<0, 1, kRowTile>(a, s);
+  return a.epilogue == 0 ? launch_typed<1, 0, kRowTile>(a, s) : launch_typed<1, 1, kRowTile>(a, s);
 }
 
 }  // namespace moe

@@ -229,7 +229,7 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   g1.num_sms = dev.num_sms;
   g1.test_stall = test_stall_producer();
   // no expert receives more than T rows (a token routes to an expert at most once)
-  g1.small_a = T <= moe::kSmallATokens ? 1 : 0;
+  g1.a_rows = (int)std::min<int64_t>(T, kRowTile);
   cudaError_t err = pair1 ? moe::launch_gemm_pair(g1, s) : moe::launch_gemm(g1, s);
   MOE_CUDA_TRY(err);
   MOE_CUDA_TRY(mark());

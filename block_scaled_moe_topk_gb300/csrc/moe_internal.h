@@ -113,10 +113,8 @@ struct GemmArgs {
   uint64_t timeout_ns;
   int num_sms;
   int test_stall;         // test hook: the producer issues nothing, so the MMA warp's wait expires
-  int small_a;            // single-CTA tiles: every tile has <= 16 routed rows (T <= 16)
+  int a_rows;             // single-CTA tiles: no tile has more routed rows (min(T, 128))
 };
-// Batches of at most this many tokens use the single-CTA GEMM's small-batch form.
-constexpr int kSmallATokens = 16;
 // gemm.cu: one CTA per 128-row x 256-column tile (any weight-scale layout).
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 // gemm_pair.cu: CTA pairs, 256-row x 256-column tiles (prepacked weight scales only).
