@@ -46,13 +46,15 @@ constexpr int kScaleWarp = 10;
 constexpr int kOutStageBytes = 32 * 32 * 2;  // GEMM2 epilogue staging: 32 rows x 32 bf16 per warp
 
 // Shared-memory geometry of one CTA.  Regular tiles stage all 128 activation rows of a tile
-// per K stage.  Small batches stage fewer -- AROWS = 16 when T <= 16, 64 when T <= 64 (no
-// tile then has more routed rows: a token routes to an expert at most once) -- which leaves
-// room for more stages of the latency-bound weight stream.  The MMA still reads 128 rows:
-// rows past AROWS come from the following bytes of the stage and only reach accumulator rows
-// that are never stored.
+// per K stage.  Small batches stage fewer, which leaves room for more stages of the
+// latency-bound weight stream: AROWS = 16 when T <= 16 (no tile then has more routed rows: a
+// token routes to an expert at most once), AROWS = 64 when experts average few rows -- work
+// units are then 64-row halves of the 128-row tiles, an expert with more than 64 rows taking
+// two.  The MMA still reads 128 rows: rows past AROWS come from the following bytes of the
+// stage and only reach accumulator rows that are never stored.
 template <int ACT, int AROWS>
 struct Geo {
+  static constexpr int kUnitRows = AROWS == 64 ? 64 : kRowTile;  // rows of one work unit
   static constexpr int kABytes = AROWS * 128;              // activation slot
   static constexpr int kBOff = kABytes;                    // weight tile, 1024-aligned (SW128)
   static constexpr int kBBytes = kNTile * 128;             // 256 rows x 128 bytes of shared memory
@@ -63,11 +65,13 @@ struct Geo {
   static constexpr int kStages = AROWS == kRowTile ? 4 : (AROWS == 16 && ACT == 0 ? 6 : 5);
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kTileBaseOff = kBarOff + 256;      // M-tile prefix over experts, int32 [E+1]
+  // 64-row units: their own prefix over experts, int32 [E+1] (else the M-tile prefix serves)
+  static constexpr int kUnitBaseOff = kTileBaseOff + 4 * (kMaxExperts + 1);
+  static constexpr int kTablesEnd = kUnitBaseOff + (kUnitRows == 64 ? 4 * (kMaxExperts + 1) : 0);
   static constexpr bool kOutStaging = AROWS == kRowTile;  // GEMM2 rows leave as TMA stores
-  static constexpr int kOutStageOff = (kTileBaseOff + 4 * (kMaxExperts + 1) + 1023) / 1024 * 1024;
+  static constexpr int kOutStageOff = (kTablesEnd + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes =
-      (kOutStaging ? kOutStageOff + kEpiWarps * kOutStageBytes : kTileBaseOff + 4 * (kMaxExperts + 1)) +
-      1024;  // + alignment slack
+      (kOutStaging ? kOutStageOff + kEpiWarps * kOutStageBytes : kTablesEnd) + 1024;  // + alignment slack
   static_assert(kBOff % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
   static_assert(kSmemBytes <= 232448, "single-CTA GEMM shared memory");
   static_assert(kStages * 32 <= 256, "TMEM scale slots");
@@ -118,11 +122,30 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + G::kBarOff + 8 * (2 * kStages + 3));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int32_t* tile_base = reinterpret_cast<int32_t*>(smem + G::kTileBaseOff);
+  // work units per expert: its M tiles, or (64-row units) ceil(count / 64)
+  int32_t* unit_base = G::kUnitRows == 64 ? reinterpret_cast<int32_t*>(smem + G::kUnitBaseOff) : tile_base;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // the per-tile expert lookup (a binary search) reads shared memory, not global memory: it
   // sits on the producer's path at every tile boundary
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) tile_base[e] = p.mtile_base[e];
+  if (G::kUnitRows == 64 && threadIdx.x / 32 == 2) {  // exclusive prefix of ceil(count / 64), warp 2
+    const int ln = threadIdx.x % 32;
+    int running = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + ln;
+      const int v = e < p.E ? (p.counts[e] + 63) / 64 : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (ln >= o) incl += n;
+      }
+      if (e < p.E) unit_base[e] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (ln == 0) unit_base[p.E] = running;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       // canonical scales: warp 0's expect_tx arrive + 32 cp.async arrivals of the scale warp;
@@ -149,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const int NT = p.N / kNTile;
   const int K = p.K;
   const int nks = (K + TR::kKPerStage - 1) / TR::kKPerStage;
-  const int64_t total_tiles = (int64_t)tile_base[p.E] * NT;
+  const int64_t total_tiles = (int64_t)unit_base[p.E] * NT;  // work units
 
   if (warp == 0 || warp == kScaleWarp) {
     // ------------------------------------------------------------------ producers
@@ -164,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
     bool ok = !p.test_stall;  // the test hook leaves every stage unfilled
     for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      const Tile tc = decode_tile(tile, tile_base, p.E, NT);
-      const int64_t row0 = ((int64_t)tile_base[tc.e] + tc.mt) * kRowTile;
+      const Tile tc = decode_tile(tile, unit_base, p.E, NT);  // tc.mt: unit index inside the expert
+      const int64_t row0 = (int64_t)tile_base[tc.e] * kRowTile + (int64_t)tc.mt * G::kUnitRows;
       const int n0 = tc.nt * kNTile;
       const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
       const int64_t sf_row32 = (int64_t)32 * (K / 32);        // 32 weight rows of scales
@@ -251,6 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       constexpr uint32_t kHalfStep = (kAtomsPerStage * 512) >> 4;  // second 128 weight rows
       const bool gathered = !p.w_sf_tiled;
       for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        // A 64-row unit over rows 64..127 of its 128-row block: the block's scale tile lands in
+        // TMEM as a whole and row m reads lane m, column sfa + m/32, so the unit's rows 0..63
+        // take the scales of block rows 64..127 two columns further on.
+        uint32_t sfa_shift = 0;
+        if (G::kUnitRows == 64) sfa_shift = 2u * (uint32_t)(decode_tile(tile, unit_base, p.E, NT).mt & 1);
         if (!lane_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
           ok = false;
           break;
@@ -284,10 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
               if (ACT == 0)
                 tc_mma_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
-                                sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * 8, acc);
+                                sf_col + (kblk >> 2) * 4 + sfa_shift, sf_col + kSfaCols + (kblk >> 2) * 8, acc);
               else
-                tc_mma_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, sf_col + (kblk >> 2) * 4,
-                            sf_col + kSfaCols + (kblk >> 2) * 8, acc);
+                tc_mma_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
+                            sf_col + (kblk >> 2) * 4 + sfa_shift, sf_col + kSfaCols + (kblk >> 2) * 8, acc);
             }
           }
           tc_commit(empty_bar(slot));
@@ -314,12 +342,21 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     const int half = (warp - 2) >> 2;  // accumulator columns [half*128, half*128 + 128)
     uint32_t acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile tc = decode_tile(tile, tile_base, p.E, NT);
-      const int row_local = tc.mt * kRowTile + quad * 32 + lane;
-      const bool valid = row_local < p.counts[tc.e];
+      const Tile tc = decode_tile(tile, unit_base, p.E, NT);
+      const int row_local = tc.mt * G::kUnitRows + quad * 32 + lane;
+      // a 64-row unit fills accumulator lanes 0..63 only: the warps of quadrants 2 and 3 keep
+      // step with the tile hand-off (wait, release) and store nothing
+      const bool lanes_used = G::kUnitRows == kRowTile || quad < 2;
+      const bool valid = lanes_used && row_local < p.counts[tc.e];
       const int64_t prow = (int64_t)tile_base[tc.e] * kRowTile + row_local;
       if (!warp_wait(tmem_full_bar, acc_phase, sync, p.timeout_ns)) break;
       tc_fence_after();
+      if (!lanes_used) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tmem_empty_bar);
+        acc_phase ^= 1u;
+        continue;
+      }
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
       float acc[128];
 #pragma unroll
@@ -450,7 +487,8 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   p.E = a.E;
   p.N = a.N;
   p.K = a.K;
-  const int64_t grid = std::min<int64_t>(a.num_sms, a.max_tiles);
+  // 64-row units: at most two per 128-row tile
+  const int64_t grid = std::min<int64_t>(a.num_sms, G::kUnitRows == 64 ? 2 * a.max_tiles : a.max_tiles);
   if (grid <= 0) return cudaSuccess;
   moe_gemm_kernel<ACT, EPI, AROWS><<<(unsigned)grid, kThreads, G::kSmemBytes, s>>>(p);
   return cudaGetLastError();
@@ -459,8 +497,8 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  // small batches (at most a_rows routed rows in any tile) stage fewer activation rows; A4W4's
-  // larger stages gain no extra stage from a 64-row slot
+  // a_rows = 16: no tile has more routed rows; 64: 64-row work units (any routing); else 128.
+  // A4W4's larger stages gain no extra stage from a 64-row slot.
   if (a.a_rows <= 16) {
     if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, 16>(a, s) : launch_typed<0, 1, 16>(a, s);
     return a.epilogue == 0 ? launch_typed<1, 0, 16>(a, s) : launch_typed<1, 1, 16>(a, s);

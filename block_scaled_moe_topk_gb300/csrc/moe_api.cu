@@ -228,8 +228,14 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   g1.timeout_ns = wait_timeout_ns();
   g1.num_sms = dev.num_sms;
   g1.test_stall = test_stall_producer();
-  // no expert receives more than T rows (a token routes to an expert at most once)
-  g1.a_rows = (int)std::min<int64_t>(T, kRowTile);
+  // T <= 16: no expert receives more than T rows (a token routes to an expert at most once);
+  // few rows per expert on average and a long K: 64-row work units
+  const bool few_rows = T * (int64_t)k <= (int64_t)moe::kUnit64MaxRowsPerExpert * E;
+  auto a_rows_for = [&](int K) {
+    if (T <= 16) return 16;
+    return few_rows && K / 128 >= moe::kUnit64MinStages ? 64 : kRowTile;
+  };
+  g1.a_rows = a_rows_for(H);
   cudaError_t err = pair1 ? moe::launch_gemm_pair(g1, s) : moe::launch_gemm(g1, s);
   MOE_CUDA_TRY(err);
   MOE_CUDA_TRY(mark());
@@ -243,6 +249,7 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   g2.N = H;
   g2.K = I;
   g2.max_tiles = mtiles_cap * (H / moe::kNTile);
+  g2.a_rows = a_rows_for(I);
   g2.out_codes = nullptr;
   g2.out_sf = nullptr;
   g2.out_bf16 = reinterpret_cast<uint16_t*>(at(L.y2));

@@ -113,8 +113,15 @@ struct GemmArgs {
   uint64_t timeout_ns;
   int num_sms;
   int test_stall;         // test hook: the producer issues nothing, so the MMA warp's wait expires
-  int a_rows;             // single-CTA tiles: no tile has more routed rows (min(T, 128))
+  int a_rows;             // single-CTA tiles: activation rows staged per K stage (16, 64 or 128;
+                          // 16 requires every tile to hold at most 16 routed rows)
 };
+// Single-CTA GEMMs stage 16 activation rows when T <= 16, and 64 rows (in 64-row work units)
+// when the batch routes at most this many rows per expert on average (T * k <= 16 * E) and the
+// GEMM's K spans at least kUnit64MinStages stages: with skewed routing or a short K, experts
+// split into two units or the per-unit overhead cost more than the deeper ring gained.
+constexpr int kUnit64MaxRowsPerExpert = 16;
+constexpr int kUnit64MinStages = 16;
 // gemm.cu: one CTA per 128-row x 256-column tile (any weight-scale layout).
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 // gemm_pair.cu: CTA pairs, 256-row x 256-column tiles (prepacked weight scales only).

@@ -372,6 +372,23 @@ def test_forward_prequant_and_ex_are_bit_identical(shape, T, act):
     assert moe.moe_read_device_status(ws) == 0
 
 
+def test_forward_64_row_units_with_a_crowded_expert():
+    """Batches that route few rows per expert on average run the GEMMs in 64-row work units; an
+    expert with more than 64 rows then takes two units, the second reading its activation
+    scales from the upper half of the 128-row scale tile.  One expert gets about half of all
+    routed rows here (T * k = 240 <= 32 * E selects the 64-row units)."""
+    T, H, I, E, k = 120, TINY.H, TINY.I, TINY.E, TINY.k
+    W = Weights(E, H, I, seed=0, device=DEV, from_bf16=True)
+    x, lg = synth.x_bf16(T, H, 9), synth.gate_logits(T, E, 9)
+    lg[:, 3] += 6.0  # expert 3 is in nearly every token's top-2
+    out, ws = _run_forward(moe.MOE_ACT_MXFP8, x, lg, W, E, k)
+    v, inv_p = _check_intermediates(moe.MOE_ACT_MXFP8, x, lg, W, E, k, ws)
+    assert v["counts"].cpu().numpy().max() > 64
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, oracle.FMT_E4M3)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
 def test_forward_independent_of_stale_workspace():
     """The padding rows of the expert segments are never written: a workspace full of stale
     random bytes gives the zeroed workspace's output bit for bit (both formats, both tilings)."""
