@@ -444,6 +444,9 @@ def run_ours(args):
                    "entry_point": "moe_a8w4_forward_prepacked",
                    "parallelism": f"dp{world} (independent token batches, no collective)"},
         "us_per_call": round(ms_per_step * 1e3, 2), "routed_rows_s": round(value * k, 1),
+        "step_us": {"p10": round(float(np.percentile(step_ms, 10)) * 1e3, 2),
+                    "median": round(statistics.median(step_ms) * 1e3, 2),
+                    "p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2)},
         "canonical_scales_us_per_call": round(canon_ms * 1e3, 2),
         "prequant_us_per_call": round(pre_ms * 1e3, 2),
         "a4w4": a4, "config_sweeps": cfg,
@@ -471,9 +474,14 @@ def cpu_baseline(x, lg, W, n_tokens, E):
     t0 = time.perf_counter()
     oracle.moe_forward(xb, lgh, *host_w, E, SHAPE.k, oracle.FMT_E4M3, nthreads=cores)
     dt = time.perf_counter() - t0
+    n1 = max(1, n_tokens // 8)  # the same oracle on one core, on a smaller sample
+    t0 = time.perf_counter()
+    oracle.moe_forward(xb[:n1], lgh[:n1], *host_w, E, SHAPE.k, oracle.FMT_E4M3, nthreads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": round(n_tokens / dt, 3), "unit": "tok/s", "cores": cores, "kind": "oracle",
             "sample": f"{n_tokens} tokens of the same batch, whole layer per token (route, quant, GEMM1, "
-                      f"SwiGLU, A2, GEMM2, combine), fp64 accumulation; {dt:.1f} s wall"}
+                      f"SwiGLU, A2, GEMM2, combine), fp64 accumulation; {dt:.1f} s wall",
+            "single_core": {"value": round(n1 / dt1, 3), "unit": "tok/s", "sample": f"{n1} tokens, {dt1:.1f} s wall"}}
 
 
 def run_reference(args):
