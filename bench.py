@@ -116,6 +116,20 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value: every timing is reduced with MAX over the ranks."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job tokens/s: the tokens all ranks processed over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 def make_workload(T, rank, device, E=SHAPE.E):
     x = synth.x_bf16(T, SHAPE.H, seed=rank, device=device)
     lg = synth.gate_logits(T, E, seed=rank, device=device)
@@ -241,11 +255,7 @@ def run_ours(args):
         return
     g = graph_for(x, lg, out)
     step_ms = timed_replays(g, args.steps, args.warmup)
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     status = moe.moe_read_device_status(ws)
     active = active_experts()
     del g
@@ -253,7 +263,7 @@ def run_ours(args):
     canon_ms = statistics.median(timed_replays(g_c, max(5, min(args.steps, 20)), 3))
     del g_c
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, T, args.steps, total_ms)
 
     # ---------------------------------------------------------------- per-kernel profile
     prof = []
@@ -337,12 +347,8 @@ def run_ours(args):
     stream.wait_stream(d2h)
     t1.record(stream)
     t1.synchronize()
-    e2e_total = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e = {"value": round(world * T * args.steps / (e2e_total / 1e3), 1), "unit": "tok/s",
+    e2e_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    e2e = {"value": round(job_throughput(world, T, args.steps, e2e_total), 1), "unit": "tok/s",
            "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4, "d2h_bytes_per_step": out.numel() * 2,
            "ms_per_step": round(e2e_total / args.steps, 4), "pipelined": True,
            "serial_ms_per_step": round(serial_ms, 4), "serial_value": round(world * T / (serial_ms / 1e3), 1)}
