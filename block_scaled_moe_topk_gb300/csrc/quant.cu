@@ -89,6 +89,61 @@ __global__ void __launch_bounds__(kQuantThreads) quant_kernel(QuantArgs a) {
   }
 }
 
+// Forward form: one block per token row, thread i owns elements [16i, 16i + 16) (lanes 2m and
+// 2m+1 share a 32-element block); the row's k destination rows are read once per thread.  No
+// grid-stride loop: every row's loads are in flight at once.
+template <int FMT>
+__global__ void __launch_bounds__(1024) quant_rows_kernel(QuantArgs a) {
+  const int K = a.K;
+  const int64_t row = blockIdx.x;
+  const int col0 = (int)threadIdx.x * 16;
+  const bool active = col0 < K;
+  float v[16];
+  if (active) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + row * K + col0);
+    const uint4 r0 = src[0], r1 = src[1];
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = 0.0f;
+  }
+  int prow[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < a.k) prow[j] = a.inv_padded[row * a.k + j];
+  float amax = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  if (!active) return;  // whole lane pairs are active or not (K % 32 == 0)
+  const MxScale sc = mx_scale<FMT>(amax);
+  const int kb = col0 / 32;
+  const bool scale_writer = (col0 & 31) == 0;
+  if (FMT == 0) {
+    const uint2 c0 = pack_e4m3x8(v, sc.mult), c1 = pack_e4m3x8(v + 8, sc.mult);
+    const uint4 c = make_uint4(c0.x, c0.y, c1.x, c1.y);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < a.k) {
+        *reinterpret_cast<uint4*>(a.codes + (int64_t)prow[j] * K + col0) = c;
+        if (scale_writer) a.scales[sf_tile_offset(prow[j], kb, K)] = sc.byte;
+      }
+  } else {
+    const uint2 c = make_uint2(pack_e2m1x8(v, sc.mult), pack_e2m1x8(v + 8, sc.mult));
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < a.k) {
+        *reinterpret_cast<uint2*>(a.codes + (int64_t)prow[j] * (K / 2) + col0 / 2) = c;
+        if (scale_writer) a.scales[sf_tile_offset(prow[j], kb, K)] = sc.byte;
+      }
+  }
+}
+
 // Canonical E8M0 scales [rows, K/32] -> the 128x4 tile layout the GEMM copies to TMEM:
 // thread i moves the 4 scale bytes (one 128-wide k-atom) of one row.
 __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* src, int64_t rows, int K, uint8_t* dst) {
@@ -145,6 +200,13 @@ cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
   const int64_t n = a.rows * (a.K / 16);
   if (n == 0) return cudaSuccess;
+  if (a.inv_padded != nullptr && a.K <= 16 * 1024 && a.rows <= 0x7fffffff) {
+    // forward: one block per token row (threads rounded up to whole warps)
+    const unsigned threads = (unsigned)((a.K / 16 + 31) / 32 * 32);
+    if (a.fmt == 0) quant_rows_kernel<0><<<(unsigned)a.rows, threads, 0, s>>>(a);
+    else quant_rows_kernel<1><<<(unsigned)a.rows, threads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   const unsigned grid = (unsigned)std::min<int64_t>((n + kQuantThreads - 1) / kQuantThreads, 152 * 8);
   if (a.fmt == 0) quant_kernel<0><<<grid, kQuantThreads, 0, s>>>(a);
   else quant_kernel<1><<<grid, kQuantThreads, 0, s>>>(a);
