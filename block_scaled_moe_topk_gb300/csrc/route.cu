@@ -1,5 +1,5 @@
-// route.cu -- top-k softmax gating, one warp per token, with the per-chunk expert
-// histogram of the routed pairs fused in.
+// route.cu -- top-k softmax gating (eight lanes per token up to 512 experts, a warp per
+// token beyond), with the per-chunk expert histogram of the routed pairs fused in.
 //
 // Gating as in "[HIP] gfx950 A8W4 fused_moe configs for DSv4.1 TP-sharded
 // experts" (Changes: the top-k softmax kernel): experts ranked by fp32 logit,
@@ -44,6 +44,32 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   }
 }
 
+// E <= 512: eight lanes per token, the block's 32 tokens in one pass (8 warps x 4 tokens).
+template <int kV>
+__global__ void __launch_bounds__(kRouteWarps * 32) route8_kernel(RouteArgs a) {
+  static_assert(kRouteWarps * 4 == kTokensPerChunk, "one pass per chunk");
+  __shared__ int hist[kV * 8];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, g = lane & 7;
+  const int E = a.E, k = a.k;
+  if (a.reset_status && blockIdx.x == 0 && threadIdx.x < 8) a.status[threadIdx.x] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t t = (int64_t)blockIdx.x * kTokensPerChunk + warp * 4 + (lane >> 3);
+  const bool valid = t < a.T;
+  int my_id;
+  float my_w;
+  route_token8<kV>(a.logits + (valid ? t : 0) * E, valid, E, k, g, my_id, my_w);
+  if (valid && g < k) {
+    a.ids[t * k + g] = my_id;
+    a.w[t * k + g] = my_w;
+    if (a.chunk_hist) atomicAdd(&hist[my_id], 1);
+  }
+  if (a.chunk_hist) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) a.chunk_hist[(int64_t)e * a.nchunk + blockIdx.x] = hist[e];
+  }
+}
+
 // Histogram of caller-supplied ids (the standalone sort entry point).
 __global__ void __launch_bounds__(256) histogram_kernel(SortArgs a) {
   __shared__ int hist[kMaxExperts];
@@ -67,8 +93,13 @@ __global__ void __launch_bounds__(256) histogram_kernel(SortArgs a) {
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   const int64_t blocks = (a.T + kTokensPerChunk - 1) / kTokensPerChunk;
   if (blocks == 0) return cudaSuccess;
-  if (a.E <= 512) route_kernel<16><<<(unsigned)blocks, kRouteWarps * 32, 0, s>>>(a);
-  else route_kernel<32><<<(unsigned)blocks, kRouteWarps * 32, 0, s>>>(a);
+  const unsigned nb = (unsigned)blocks, nt = kRouteWarps * 32;
+  if (a.E <= 64) route8_kernel<8><<<nb, nt, 0, s>>>(a);
+  else if (a.E <= 128) route8_kernel<16><<<nb, nt, 0, s>>>(a);
+  else if (a.E <= 256) route8_kernel<32><<<nb, nt, 0, s>>>(a);
+  else if (a.E <= 384) route8_kernel<48><<<nb, nt, 0, s>>>(a);
+  else if (a.E <= 512) route8_kernel<64><<<nb, nt, 0, s>>>(a);
+  else route_kernel<32><<<nb, nt, 0, s>>>(a);
   return cudaGetLastError();
 }
 

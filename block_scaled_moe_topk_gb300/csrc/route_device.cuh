@@ -87,4 +87,82 @@ __device__ __forceinline__ void route_token(const float* l, int E, int k, int la
   w_out = __fdiv_rn(p, zh) * (1.0f - __fdiv_rn(zl, zh));
 }
 
+// Eight lanes per token (lane g = lane % 8 of its group holds experts g + 8 i, i < kV), so a
+// warp routes four tokens at once with three butterfly levels per selection instead of five.
+// Same ranking and weights as route_token; kV >= ceil(E / 8), kV <= 64.  The local scan runs
+// as two interleaved chains (even and odd i) to halve its dependency length.  Experts past E
+// and the tokens of an invalid group hold NaN, which no comparison selects.
+template <int kV>
+__device__ __forceinline__ void route_token8(const float* l, bool valid, int E, int k, int g, int& id_out,
+                                             float& w_out) {
+  static_assert(kV % 2 == 0 && kV <= 64, "values per lane");
+  constexpr int kNone = 0x7fffffff;
+  const float nan = __int_as_float(0x7fc00000);
+  float v[kV];
+#pragma unroll
+  for (int i = 0; i < kV; ++i) {
+    const int e = g + 8 * i;
+    v[i] = (valid && e < E) ? l[e] : nan;
+  }
+  uint64_t taken = 0;
+  int my_id = 0;
+  float my_val = 0.0f, lmax = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    float b0 = -INFINITY, b1 = -INFINITY;
+    int i0 = kNone, i1 = kNone;
+#pragma unroll
+    for (int i = 0; i < kV; i += 2) {
+      if (!((taken >> i) & 1ull) && route_better(v[i], g + 8 * i, b0, i0)) {
+        b0 = v[i];
+        i0 = g + 8 * i;
+      }
+      if (!((taken >> (i + 1)) & 1ull) && route_better(v[i + 1], g + 8 * (i + 1), b1, i1)) {
+        b1 = v[i + 1];
+        i1 = g + 8 * (i + 1);
+      }
+    }
+    float bv = b0;
+    int bi = i0;
+    if (route_better(b1, i1, bv, bi)) {
+      bv = b1;
+      bi = i1;
+    }
+    // arg-max over the group's eight lanes (value desc, index asc); (-inf, kNone) is "none"
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (route_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi != kNone && (bi & 7) == g) taken |= 1ull << (bi >> 3);
+    if (j == 0) lmax = bv;
+    if (g == j) {
+      my_id = bi;
+      my_val = bv;
+    }
+  }
+  float p = 0.0f;  // exp(l_j - l_max) as in route_token
+  if (g < k) {
+    const float sdiff = my_val - lmax;
+    const float bb = sdiff - my_val;
+    const float e = (my_val - (sdiff - bb)) + (-lmax - bb);
+    p = expf(sdiff) * (1.0f + e);
+  }
+  float zh = p, zl = 0.0f;  // compensated sum over the group
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, zh, off);
+    const float ol = __shfl_xor_sync(0xffffffffu, zl, off);
+    const float sum = zh + oh;
+    const float bv = sum - zh;
+    zl += ol + ((zh - (sum - bv)) + (oh - bv));
+    zh = sum;
+  }
+  id_out = my_id;
+  w_out = __fdiv_rn(p, zh) * (1.0f - __fdiv_rn(zl, zh));
+}
+
 }  // namespace moe

@@ -7,10 +7,10 @@
 //
 // Three phases, no atomics on the output order:
 //   1. per-chunk expert histograms (route.cu, fused into the routing kernel);
-//   2. one block: per-expert exclusive prefix over chunks, then prefixes over
-//      experts -> counts, offsets, 128-row padded offsets, M-tile bases;
-//   3. one warp per chunk walks its pairs in order and places each at
-//      offset[e] + chunk_base[e] + rank, so equal experts keep pair order.
+//   2. a warp per expert: exclusive prefix over chunks -> chunk bases, counts;
+//   3. a warp per chunk: prefixes over experts -> offsets, 128-row padded offsets,
+//      M-tile bases (written once), then it walks its pairs in order and places each
+//      at offset[e] + chunk_base[e] + rank, so equal experts keep pair order.
 #include "moe_internal.h"
 #include "route_device.cuh"
 
@@ -47,65 +47,83 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* warp_tot, int64_t* t
   return r;
 }
 
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(SortArgs a) {
-  __shared__ int cnt[kMaxExperts];
-  __shared__ int64_t warp_tot[32];
-  __shared__ int64_t total;
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  const int E = a.E;
+// Phase 2a: one warp per expert turns its row of per-chunk counts into exclusive per-chunk
+// bases (in place) and writes the expert's total to counts[e].  Rows are independent, so
+// the experts spread over E / 8 blocks.
+constexpr int kColWarps = 8;
+
+__global__ void __launch_bounds__(kColWarps * 32) scan_cols_kernel(SortArgs a) {
+  const int lane = threadIdx.x % 32;
+  const int e = blockIdx.x * kColWarps + threadIdx.x / 32;
+  if (e >= a.E) return;
   const int64_t nchunk = a.nchunk;
-  // per expert: exclusive prefix over chunks, in place; 8 rows of 32 chunks are loaded
-  // before any is scanned so the loads overlap instead of forming a latency chain
+  int32_t* col = a.chunk_hist + (int64_t)e * nchunk;
+  int running = 0;
+  // 8 runs of 32 chunks are loaded before any is scanned, so the loads overlap
   constexpr int kRounds = 8;
-  for (int e = warp; e < E; e += kScanThreads / 32) {
-    int32_t* col = a.chunk_hist + (int64_t)e * nchunk;
-    int running = 0;
-    for (int64_t b0 = 0; b0 < nchunk; b0 += 32 * kRounds) {
-      int v[kRounds];
+  for (int64_t b0 = 0; b0 < nchunk; b0 += 32 * kRounds) {
+    int v[kRounds];
 #pragma unroll
-      for (int r = 0; r < kRounds; ++r) {
-        const int64_t b = b0 + 32 * r + lane;
-        v[r] = (b < nchunk) ? col[b] : 0;
-      }
-#pragma unroll
-      for (int r = 0; r < kRounds; ++r) {
-        const int64_t b = b0 + 32 * r + lane;
-        const int incl = warp_inclusive_scan<int>(v[r], lane);
-        if (b < nchunk) col[b] = running + incl - v[r];
-        running += __shfl_sync(0xffffffffu, incl, 31);
-      }
+    for (int r = 0; r < kRounds; ++r) {
+      const int64_t b = b0 + 32 * r + lane;
+      v[r] = (b < nchunk) ? col[b] : 0;
     }
-    if (lane == 0) cnt[e] = running;
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int64_t b = b0 + 32 * r + lane;
+      const int incl = warp_inclusive_scan<int>(v[r], lane);
+      if (b < nchunk) col[b] = running + incl - v[r];
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
   }
-  __syncthreads();
-  const int e = threadIdx.x;
-  const int c = (e < E) ? cnt[e] : 0;
-  const int64_t off = block_exclusive_scan(c, warp_tot, &total);
-  const int64_t tot_rows = total;
-  const int64_t padded = ((int64_t)c + kRowTile - 1) / kRowTile * kRowTile;
-  const int64_t poff = block_exclusive_scan(padded, warp_tot, &total);
-  const int64_t tot_padded = total;
-  const int64_t tiles = padded / kRowTile;
-  const int64_t toff = block_exclusive_scan(tiles, warp_tot, &total);
-  const int64_t tot_tiles = total;
-  if (e < E) {
-    a.counts[e] = c;
-    a.offsets[e] = off;
-    if (a.padded_offsets) a.padded_offsets[e] = poff;
-    if (a.mtile_base) a.mtile_base[e] = (int32_t)toff;
-  }
-  if (e == 0) {
-    a.offsets[E] = tot_rows;
-    if (a.padded_offsets) a.padded_offsets[E] = tot_padded;
-    if (a.mtile_base) a.mtile_base[E] = (int32_t)tot_tiles;
-  }
+  if (lane == 0) a.counts[e] = running;
 }
 
+// Phase 2b + 3, one warp per chunk.  The warp first forms the exclusive prefixes over experts
+// of the routed rows and of the 128-row padded rows from counts[] (every chunk's warp does
+// this for itself; chunk 0's also writes offsets, padded offsets and M-tile bases), then walks
+// its pairs in order and places each at offset[e] + chunk_base[e] + rank, so equal experts
+// keep pair order.  Dynamic shared memory: E x (int64 offset, int64 padded offset, int32 next).
 __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
-  __shared__ int next[kMaxExperts];
+  extern __shared__ __align__(8) uint8_t sort_smem[];
   const int lane = threadIdx.x;
   const int E = a.E, k = a.k;
+  int64_t* off_s = reinterpret_cast<int64_t*>(sort_smem);
+  int64_t* poff_s = off_s + E;
+  int* next = reinterpret_cast<int*>(poff_s + E);
   const int64_t b = blockIdx.x;
+  for (int e = lane; e < E; e += 32) next[e] = a.counts[e];
+  __syncwarp();
+  // lane L owns experts [L * per, L * per + per)
+  const int per = (E + 31) / 32;
+  const int e0 = min(lane * per, E), e1 = min(e0 + per, E);
+  int64_t s = 0, sp = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int64_t c = next[e];
+    s += c;
+    sp += (c + kRowTile - 1) / kRowTile * kRowTile;
+  }
+  int64_t xs = warp_inclusive_scan<int64_t>(s, lane) - s;
+  int64_t xsp = warp_inclusive_scan<int64_t>(sp, lane) - sp;
+  const bool head = b == 0;
+  for (int e = e0; e < e1; ++e) {
+    const int64_t c = next[e];
+    off_s[e] = xs;
+    poff_s[e] = xsp;
+    if (head) {
+      a.offsets[e] = xs;
+      if (a.padded_offsets) a.padded_offsets[e] = xsp;
+      if (a.mtile_base) a.mtile_base[e] = (int32_t)(xsp / kRowTile);
+    }
+    xs += c;
+    xsp += (c + kRowTile - 1) / kRowTile * kRowTile;
+  }
+  if (head && lane == 31) {  // lane 31 ends at the totals
+    a.offsets[E] = xs;
+    if (a.padded_offsets) a.padded_offsets[E] = xsp;
+    if (a.mtile_base) a.mtile_base[E] = (int32_t)(xsp / kRowTile);
+  }
+  __syncwarp();
   for (int e = lane; e < E; e += 32) next[e] = a.chunk_hist[(int64_t)e * a.nchunk + b];
   __syncwarp();
   const int64_t q_begin = b * kTokensPerChunk * k;
@@ -126,10 +144,10 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
     __syncwarp();
     if (valid) {
       const int64_t local = (int64_t)base + rank;
-      const int64_t r = a.offsets[id] + local;
+      const int64_t r = off_s[id] + local;
       a.sorted_pair[r] = (int32_t)q;
       a.inv[q] = (int32_t)r;
-      if (a.inv_padded) a.inv_padded[q] = (int32_t)(a.padded_offsets[id] + local);
+      if (a.inv_padded) a.inv_padded[q] = (int32_t)(poff_s[id] + local);
     }
   }
 }
@@ -228,13 +246,14 @@ cudaError_t launch_route_sort_small(const RouteArgs& ra, const SortArgs& sa, cud
 
 cudaError_t launch_scan(const SortArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  scan_kernel<<<1, kScanThreads, 0, s>>>(a);
+  scan_cols_kernel<<<(unsigned)((a.E + kColWarps - 1) / kColWarps), kColWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_scatter(const SortArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  scatter_kernel<<<(unsigned)a.nchunk, 32, 0, s>>>(a);
+  const size_t smem = (size_t)a.E * (2 * sizeof(int64_t) + sizeof(int));  // <= 20 KB
+  scatter_kernel<<<(unsigned)a.nchunk, 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
