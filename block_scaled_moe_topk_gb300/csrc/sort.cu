@@ -29,24 +29,6 @@ __device__ __forceinline__ T warp_inclusive_scan(T v, int lane) {
   return v;
 }
 
-// Exclusive block-wide prefix of one int64 value per thread (kScanThreads threads).
-__device__ int64_t block_exclusive_scan(int64_t v, int64_t* warp_tot, int64_t* total) {
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  const int64_t incl = warp_inclusive_scan<int64_t>(v, lane);
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int64_t wv = warp_tot[lane];
-    const int64_t wincl = warp_inclusive_scan<int64_t>(wv, lane);
-    warp_tot[lane] = wincl - wv;
-    if (lane == 31) *total = wincl;
-  }
-  __syncthreads();
-  const int64_t r = warp_tot[warp] + incl - v;
-  __syncthreads();
-  return r;
-}
-
 // Phase 2a: one warp per expert turns its row of per-chunk counts into exclusive per-chunk
 // bases (in place) and writes the expert's total to counts[e].  Rows are independent, so
 // the experts spread over E / 8 blocks.
@@ -154,7 +136,7 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
 
 // Small batches (T <= kSmallRouteTokens): routing, histogram, the prefix sums and the stable
 // scatter in one block, so a decode step pays one launch instead of three.  Same results as
-// route_kernel + scan_kernel + scatter_kernel.
+// the routing kernel + scan_cols_kernel + scatter_kernel.
 constexpr int kSmallMaxRows = kSmallRouteTokens * kMaxTopK;
 
 template <int kPerLane>
@@ -164,8 +146,6 @@ __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArg
   __shared__ int64_t off_s[kMaxExperts];
   __shared__ int64_t poff_s[kMaxExperts];
   __shared__ int ids_s[kSmallMaxRows];
-  __shared__ int64_t warp_tot[32];
-  __shared__ int64_t total;
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   const int E = ra.E, k = ra.k;
   const int64_t T = ra.T;
@@ -187,30 +167,39 @@ __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArg
     }
   }
   __syncthreads();
-  const int e = threadIdx.x;
-  const int c = (e < E) ? cnt[e] : 0;
-  const int64_t off = block_exclusive_scan(c, warp_tot, &total);
-  const int64_t tot_rows = total;
-  const int64_t padded = ((int64_t)c + kRowTile - 1) / kRowTile * kRowTile;
-  const int64_t poff = block_exclusive_scan(padded, warp_tot, &total);
-  const int64_t tot_padded = total;
-  const int64_t toff = block_exclusive_scan(padded / kRowTile, warp_tot, &total);
-  const int64_t tot_tiles = total;
-  if (e < E) {
-    sa.counts[e] = c;
-    sa.offsets[e] = off;
-    sa.padded_offsets[e] = poff;
-    sa.mtile_base[e] = (int32_t)toff;
-    off_s[e] = off;
-    poff_s[e] = poff;
+  if (warp != 0) return;
+  // Warp 0 alone from here: the prefixes over experts (lane L owns experts [L * per, L * per +
+  // per)), then the stable scatter; no block-wide barrier on a decode step's critical path.
+  {
+    const int per = (E + 31) / 32;
+    const int e0 = min(lane * per, E), e1 = min(e0 + per, E);
+    int64_t sum = 0, psum = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int64_t c = cnt[e];
+      sum += c;
+      psum += (c + kRowTile - 1) / kRowTile * kRowTile;
+    }
+    int64_t xs = warp_inclusive_scan<int64_t>(sum, lane) - sum;
+    int64_t xps = warp_inclusive_scan<int64_t>(psum, lane) - psum;
+    for (int e = e0; e < e1; ++e) {
+      const int c = cnt[e];
+      sa.counts[e] = c;
+      sa.offsets[e] = xs;
+      sa.padded_offsets[e] = xps;
+      sa.mtile_base[e] = (int32_t)(xps / kRowTile);
+      off_s[e] = xs;
+      poff_s[e] = xps;
+      xs += c;
+      xps += ((int64_t)c + kRowTile - 1) / kRowTile * kRowTile;
+    }
+    if (lane == 31) {  // lane 31 ends at the totals
+      sa.offsets[E] = xs;
+      sa.padded_offsets[E] = xps;
+      sa.mtile_base[E] = (int32_t)(xps / kRowTile);
+    }
   }
-  if (e == 0) {
-    sa.offsets[E] = tot_rows;
-    sa.padded_offsets[E] = tot_padded;
-    sa.mtile_base[E] = (int32_t)tot_tiles;
-  }
-  __syncthreads();
-  if (warp == 0) {  // stable scatter, pairs in ascending order
+  __syncwarp();
+  {  // stable scatter, pairs in ascending order
     const int64_t R = T * k;
     const uint32_t lt_mask = (1u << lane) - 1u;
     for (int64_t q0 = 0; q0 < R; q0 += 32) {

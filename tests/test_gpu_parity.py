@@ -28,7 +28,12 @@ def _lib():
 
 # --------------------------------------------------------------------------- routing
 @pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (300, 64, 6, False), (4096, 384, 6, False),
-                                        (2000, 128, 3, True), (77, 1024, 8, False), (33, 5, 5, False)])
+                                        (2000, 128, 3, True), (77, 1024, 8, False), (33, 5, 5, False),
+                                        # each per-lane width of the eight-lanes-per-token kernel
+                                        # (E <= 64, 128, 256, 384, 512) at and past its edge, and
+                                        # the first expert count routed a warp per token (513)
+                                        (130, 65, 4, False), (250, 256, 8, False), (99, 257, 6, True),
+                                        (1000, 512, 4, False), (61, 513, 2, True)])
 def test_route_bit_exact(T, E, k, skew):
     lg = synth.gate_logits(T, E, seed=T + E, skew=skew)
     lg[0, :] = 0.25  # a fully tied row
@@ -44,7 +49,8 @@ def test_route_bit_exact(T, E, k, skew):
 
 # --------------------------------------------------------------------------- sort
 @pytest.mark.parametrize("T,E,k,skew", [(1, 384, 6, False), (257, 8, 2, False), (8192, 384, 6, False),
-                                        (32768, 384, 6, True), (5000, 128, 3, True)])
+                                        (32768, 384, 6, True), (5000, 128, 3, True), (3000, 1000, 4, True),
+                                        (40, 1024, 8, False)])
 def test_sort_bit_exact(T, E, k, skew):
     lg = synth.gate_logits(T, E, seed=3, skew=skew)
     ids_h, _ = oracle.route(lg.numpy(), k)
