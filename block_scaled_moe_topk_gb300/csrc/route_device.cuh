@@ -16,7 +16,9 @@ __device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// Lane j < k of the calling warp receives slot j: expert id and renormalised weight.
+// Lane j < k of the calling warp receives slot j: expert id and renormalised weight.  NaN
+// logits (outside what the method defines) rank as -inf, lowest index first among equals, so
+// the ids are always k distinct experts.
 // kMaxPerLane >= ceil(E / 32): logits held per lane (fewer registers for smaller E).
 template <int kMaxPerLane = kMaxExperts / 32>
 __device__ __forceinline__ void route_token(const float* l, int E, int k, int lane, int& id_out, float& w_out) {
@@ -26,7 +28,8 @@ __device__ __forceinline__ void route_token(const float* l, int E, int k, int la
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (i < per_lane && e < E) ? l[e] : 0.0f;
+    const float x = (i < per_lane && e < E) ? l[e] : 0.0f;
+    v[i] = x != x ? -INFINITY : x;  // a NaN logit ranks as -inf (below every number)
   }
   uint32_t taken = 0;
   int my_id = 0;
@@ -70,7 +73,8 @@ __device__ __forceinline__ void route_token(const float* l, int E, int k, int la
     const float sdiff = my_val - lmax;
     const float bb = sdiff - my_val;
     const float e = (my_val - (sdiff - bb)) + (-lmax - bb);
-    p = expf(sdiff) * (1.0f + e);
+    // an expert infinitely far below the maximum weighs exactly 0 (the two-sum term is NaN there)
+    p = sdiff == -INFINITY ? 0.0f : expf(sdiff) * (1.0f + e);
   }
   // z = sum of the k values as a compensated (hi, lo) pair, so w = p / z loses <= 1 ulp
   float zh = p, zl = 0.0f;
@@ -102,7 +106,10 @@ __device__ __forceinline__ void route_token8(const float* l, bool valid, int E, 
 #pragma unroll
   for (int i = 0; i < kV; ++i) {
     const int e = g + 8 * i;
-    v[i] = (valid && e < E) ? l[e] : nan;
+    const float x = (valid && e < E) ? l[e] : nan;
+    // a NaN logit ranks as -inf, so a valid token always finds k experts; only the padding
+    // (experts past E, tokens past T) stays NaN and is never selected
+    v[i] = (valid && e < E && x != x) ? -INFINITY : x;
   }
   uint64_t taken = 0;
   int my_id = 0;
@@ -149,7 +156,7 @@ __device__ __forceinline__ void route_token8(const float* l, bool valid, int E, 
     const float sdiff = my_val - lmax;
     const float bb = sdiff - my_val;
     const float e = (my_val - (sdiff - bb)) + (-lmax - bb);
-    p = expf(sdiff) * (1.0f + e);
+    p = sdiff == -INFINITY ? 0.0f : expf(sdiff) * (1.0f + e);
   }
   float zh = p, zl = 0.0f;  // compensated sum over the group
 #pragma unroll

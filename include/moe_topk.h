@@ -156,7 +156,9 @@ size_t moe_workspace_bytes(int64_t T, int H, int I, int E, int k, moe_act_fmt_t 
  * logits (the full softmax denominator cancels).
  *   gate_logits  fp32 [T, E] row-major, device
  *   topk_ids     int32 [T, k] out, device;  topk_w fp32 [T, k] out, device
- * 1 <= k <= 8, k <= E <= 1024, T >= 0 (T = 0 is a no-op).
+ * 1 <= k <= 8, k <= E <= 1024, T >= 0 (T = 0 is a no-op).  A NaN logit ranks as
+ * -inf (the method defines none), so topk_ids always holds k distinct experts;
+ * the forward entry points route the same way.
  */
 moe_status_t moe_topk_route(const float* gate_logits, int64_t T, int E, int k, int32_t* topk_ids,
                             float* topk_w, void* stream);

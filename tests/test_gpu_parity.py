@@ -47,6 +47,38 @@ def test_route_bit_exact(T, E, k, skew):
     np.testing.assert_allclose(w.cpu().numpy(), want_w, rtol=1e-6, atol=0)
 
 
+@pytest.mark.parametrize("E,k", [(384, 6), (1024, 8)])
+def test_route_nan_logits_rank_as_minus_infinity(E, k):
+    """NaN logits rank as -inf, lower index first among them, so every id is a valid distinct
+    expert even for a row with fewer than k numbers; the forward's own routing (small-batch
+    kernel) agrees."""
+    T = 40
+    lg = synth.gate_logits(T, E, seed=21)
+    lg[0, :] = float("nan")
+    lg[0, [5, 200 % E]] = 1.0          # two numbers, then the lowest-index NaNs
+    lg[1, ::3] = float("nan")
+    lg[2, :] = float("nan")            # no number at all: experts 0..k-1 in order
+    want_ids, want_w = oracle.route(np.where(np.isnan(lg.numpy()), -np.inf, lg.numpy()).astype(np.float32), k)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    moe.moe_topk_route(lg.to(DEV), k, ids, w)
+    got = ids.cpu().numpy()
+    assert np.array_equal(got, want_ids)
+    assert np.array_equal(got[2], np.arange(k))
+    ok = np.isfinite(want_w).all(1)      # rows whose kept logits are all -inf have no weights
+    np.testing.assert_allclose(w.cpu().numpy()[ok], want_w[ok], rtol=1e-6, atol=0)
+    # the forward (T <= 64: one-block route + sort) routes the same way
+    H, I = 256, 128
+    W = Weights(E, H, I, seed=0, device=DEV, from_bf16=True)
+    x = synth.x_bf16(T, H, 21)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(T, H, I, E, k), dtype=torch.uint8, device=DEV)
+    moe.moe_a8w4_forward(x.to(DEV), lg.to(DEV), *W.dev, out, E, k, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    assert np.array_equal(moe.workspace_views(ws, T, H, I, E, k)["topk_ids"].cpu().numpy(), want_ids)
+
+
 # --------------------------------------------------------------------------- sort
 @pytest.mark.parametrize("T,E,k,skew", [(1, 384, 6, False), (257, 8, 2, False), (8192, 384, 6, False),
                                         (32768, 384, 6, True), (5000, 128, 3, True), (3000, 1000, 4, True),
