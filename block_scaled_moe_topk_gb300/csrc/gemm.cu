@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gemm_common.cuh"
@@ -417,15 +418,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 template <int ACT, int EPI, int AROWS>
 cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   using G = Geo<ACT, AROWS>;
-  static bool attr_set[64] = {};
+  // per device, set once; host threads racing here both set the same attribute
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     err = cudaFuncSetAttribute(moe_gemm_kernel<ACT, EPI, AROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                G::kSmemBytes);
     if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   EncodeTiledFn encode = get_encode_fn();
   if (!encode) return cudaErrorNotSupported;

@@ -27,6 +27,7 @@
 // cluster barrier before the pair's TMEM is freed.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gemm_common.cuh"
@@ -376,7 +377,8 @@ CUresult encode_scale_rows(EncodeTiledFn encode, CUtensorMap* m, const uint8_t* 
 
 template <int ACT, int EPI>
 cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
-  static int max_clusters[64] = {};
+  // per device, computed once; host threads racing here compute and store the same value
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -392,7 +394,7 @@ cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters[dev] == 0) {
+  if (max_clusters[dev].load(std::memory_order_acquire) == 0) {
     err = cudaFuncSetAttribute(moe_gemm_pair_kernel<ACT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kPSmemBytes);
     if (err != cudaSuccess) return err;
@@ -401,7 +403,7 @@ cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
     err = cudaOccupancyMaxActiveClusters(&n, moe_gemm_pair_kernel<ACT, EPI>, &cfg);
     if (err != cudaSuccess) return err;
     if (n <= 0) return cudaErrorInvalidConfiguration;
-    max_clusters[dev] = n;
+    max_clusters[dev].store(n, std::memory_order_release);
   }
   EncodeTiledFn encode = get_encode_fn();
   if (!encode) return cudaErrorNotSupported;
@@ -457,7 +459,7 @@ cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
   p.K = a.K;
   p.test_stall = a.test_stall;
   // pair tiles <= M tiles: a bound on the clusters that can find work
-  const int64_t clusters = std::min<int64_t>(max_clusters[dev], a.max_tiles);
+  const int64_t clusters = std::min<int64_t>(max_clusters[dev].load(std::memory_order_acquire), a.max_tiles);
   if (clusters <= 0) return cudaSuccess;
   cfg.gridDim = dim3((unsigned)(2 * clusters));
   err = cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<ACT, EPI>, p);
