@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -74,7 +75,9 @@ class Clocks:
 
     def __init__(self, device_index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        # raw samples go to MOE_BENCH_CLOCKS_DIR if set (to keep them), else to a temporary folder
+        out_dir = os.environ.get("MOE_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"moe_bench_clocks_rank{device_index}.csv")
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
             sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
