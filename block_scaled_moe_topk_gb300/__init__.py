@@ -14,8 +14,7 @@ import os
 import torch
 
 __all__ = [
-    "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "MOE_GEMM_TILES_AUTO", "MOE_GEMM_TILES_SINGLE",
-    "MOE_GEMM_TILES_PAIR", "lib", "moe_status_string", "moe_workspace_bytes",
+    "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "MOE_SCHEDULE_AUTO", "MOE_SCHEDULE_CHAIN", "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
     "moe_quantize_mx", "moe_a8w4_forward",
     "moe_a4w4_forward", "moe_forward_ex", "moe_a8w4_forward_prequant", "moe_a4w4_forward_prequant", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
@@ -25,9 +24,8 @@ __all__ = [
 
 MOE_ACT_MXFP8 = 0
 MOE_ACT_MXFP4 = 1
-MOE_GEMM_TILES_AUTO = 0    # single tiles (fastest on every measured shape)
-MOE_GEMM_TILES_SINGLE = 1  # one CTA per 128 x 256 tile
-MOE_GEMM_TILES_PAIR = 2    # two CTAs (cta_group::2) per 256 x 256 tile; prepacked scales only
+MOE_SCHEDULE_AUTO = 0   # the library's choice for the shape and T
+MOE_SCHEDULE_CHAIN = 1  # kernel chain, one CTA per 128 x 256 GEMM tile over the whole K
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_topk.so")
 
 STATUS_NAMES = {
@@ -55,7 +53,7 @@ class ForwardArgs(ctypes.Structure):
                 ("w1", ctypes.c_void_p), ("w1_scale", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("w2_scale", ctypes.c_void_p), ("out", ctypes.c_void_p), ("T", ctypes.c_int64), ("H", ctypes.c_int),
                 ("I", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p), ("gemm_tiles", ctypes.c_int)]
+                ("workspace_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p), ("schedule", ctypes.c_int)]
 
 
 _lib = None
@@ -216,9 +214,9 @@ def moe_a4w4_forward_prequant(xq, xq_scale, gate_logits, w1, w1_scale, w2, w2_sc
 
 
 def moe_forward_ex(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, act_fmt=MOE_ACT_MXFP8,
-                   x_scale=None, weight_scales_prepacked=False, stream=None, gemm_tiles=MOE_GEMM_TILES_AUTO):
+                   x_scale=None, weight_scales_prepacked=False, stream=None, schedule=MOE_SCHEDULE_AUTO):
     """Any forward variant: bf16 x (x_scale None) or prequantised codes + scales; canonical or
-    prepacked weight scales; the GEMM tiling (MOE_GEMM_TILES_*)."""
+    prepacked weight scales; the schedule (MOE_SCHEDULE_*)."""
     T, H = out.shape
     a = ForwardArgs(act_fmt=int(act_fmt), prequantized=int(x_scale is not None),
                     weight_scales_prepacked=int(bool(weight_scales_prepacked)), x=x.data_ptr(),
@@ -226,7 +224,7 @@ def moe_forward_ex(x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, worksp
                     w1=w1.data_ptr(), w1_scale=w1_scale.data_ptr(), w2=w2.data_ptr(), w2_scale=w2_scale.data_ptr(),
                     out=out.data_ptr(), T=T, H=H, I=w2.shape[-1] * 2, E=int(E), k=int(k),
                     workspace=workspace.data_ptr(), workspace_bytes=workspace.numel() * workspace.element_size(),
-                    stream=_stream(stream).value, gemm_tiles=int(gemm_tiles))
+                    stream=_stream(stream).value, schedule=int(schedule))
     _check(lib().moe_forward_ex(ctypes.byref(a)), "moe_forward_ex")
 
 
@@ -255,7 +253,7 @@ KERNEL_NAMES_SMALL = ("route_sort", "quant", "gemm1", "gemm2", "combine")  # T <
 
 
 def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None,
-                        prepacked_scales=False, gemm_tiles=MOE_GEMM_TILES_AUTO):
+                        prepacked_scales=False, schedule=MOE_SCHEDULE_AUTO):
     """One forward with a CUDA event between kernels; returns {kernel name: microseconds}."""
     T, H = x.shape
     I = w2.shape[-1] * 2
@@ -264,7 +262,7 @@ def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E,
     _check(lib().moe_profile_forward(int(fmt), _p(x), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale),
                                      _p(out), T, H, I, int(E), int(k), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream),
-                                     int(bool(prepacked_scales)), int(gemm_tiles), us),
+                                     int(bool(prepacked_scales)), int(schedule), us),
            "moe_profile_forward")
     names = KERNEL_NAMES if n == len(KERNEL_NAMES) else KERNEL_NAMES_SMALL
     return {names[i]: float(us[i]) for i in range(n)}

@@ -1,8 +1,8 @@
 // combine.cu -- top-k weighted combine back to token order.
 //
 // out[t, n] = bf16_rne( sum_{j<k} topk_w[t, j] * y2[inv_padded[t*k + j], n] ), accumulated in
-// fp32 in slot order ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical
-// Details: "accumulate TopK contributions in FP32"); y2 rows are bf16.  Each thread owns 8
+// fp32 in slot order: the page "add A4W4 and FP8 P2P transport support to MegaMoE" (Technical
+// Details) sums the top-k contributions of a token in single precision; y2 rows are bf16.  Each thread owns 8
 // consecutive columns: one 16-byte load per slot, one 16-byte bf16 store.
 #include <cuda_bf16.h>
 

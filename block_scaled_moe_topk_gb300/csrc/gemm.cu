@@ -4,8 +4,9 @@
 //   GEMM1 (EPI=0): acc[r, n] = sum_K xq[r, K] * W1[e, n, K], n in [0, 2I) with rows 2j = gate_j,
 //                  2j+1 = up_j ("feat(moe): FlyDSL MegaMoE fused EP-MoE integration", description:
 //                  INTERLEAVE(g1u1)); the epilogue forms h_j = silu(gate_j) * up_j and requantises
-//                  h to MX (A2: "add A4W4 and FP8 P2P transport support to MegaMoE", Technical
-//                  Details: "emit FP4 A2 activations/scales"; E4M3 codes for A8W4).
+//                  h to MX: the intermediate activation A2 leaves as FP4 codes with E8M0 scales
+//                  for A4W4 ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical
+//                  Details) and as E4M3 codes for A8W4.
 //   GEMM2 (EPI=1): y2[r, n] = sum_I a2[r, I] * W2[e, n, I], accumulated in fp32, stored as bf16.
 //
 // Tiles are 128 routed rows (one expert's padded segment) x 256 output columns.  Per CTA:
@@ -170,7 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const uint32_t tmem_base = *tmem_holder;
 
   const Sync sync{abort_flag, p.status, p.timeout_ns, bar0};
-  const int NT = p.N / kNTile;
+  // N is a multiple of 128: when it is not one of 256 the last N tile has 128 columns.  Its
+  // weight rows past N come from the TMA's out-of-bounds zero fill, its scale copies stop at N
+  // and the epilogue warps of the missing half store nothing.
+  const int NT = (p.N + kNTile - 1) / kNTile;
   const int K = p.K;
   const int nks = (K + TR::kKPerStage - 1) / TR::kKPerStage;
   const int64_t total_tiles = (int64_t)unit_base[p.E] * NT;  // work units
@@ -194,9 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
       const int64_t sf_row32 = (int64_t)32 * (K / 32);        // 32 weight rows of scales
       const uint8_t* lane_sf = wsf_rows + (int64_t)lane * (K / 32);
+      const int n_rows = min(kNTile, p.N - n0);  // weight rows of this tile inside [0, N)
       if (!tma_warp && !p.w_sf_tiled && lane == 0) {
         // warm L2 with this tile's whole (contiguous) weight-scale block
-        const uint32_t sf_bytes = (uint32_t)kNTile * (uint32_t)(K / 32);
+        const uint32_t sf_bytes = (uint32_t)n_rows * (uint32_t)(K / 32);
         if ((reinterpret_cast<uintptr_t>(wsf_rows) & 15) == 0 && (sf_bytes & 15) == 0)
           bulk_prefetch_l2(wsf_rows, sf_bytes);
       }
@@ -219,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           } else if (p.w_sf_tiled) {
             // weight side with prepacked scales: codes + one contiguous run of k-atoms per
             // 128-row half of the tile, issued in parallel with warp 0
-            mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(TR::kBTxBytes + 2 * katoms * 512));
+            const int halves = n_rows > 128 ? 2 : 1;
+            mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(TR::kBTxBytes + halves * katoms * 512));
             tma_load_3d(st + G::kBOff, &p.tmap_w, full_bar(slot), ks * 128, n0, tc.e);
-#pragma unroll
-            for (int na = 0; na < 2; ++na)
+            for (int na = 0; na < halves; ++na)
               bulk_load(st + kSfbOff + na * (kAtomsPerStage * 512),
                         p.w_sf + ((((int64_t)tc.e * p.N + n0) / 128 + na) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
                         (uint32_t)katoms * 512u, full_bar(slot));
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 #pragma unroll
           for (int j = 0; j < 8 * kAtomsPerStage; ++j) {
             const int jj = j & 7, ka = j >> 3;
-            if (ka < katoms)
+            if (ka < katoms && jj * 32 + lane < n_rows)
               cp_async_4(dst_k + (jj >> 2) * (kAtomsPerStage * 512) + ka * 512 + (jj & 3) * 4,
                          src_k + jj * sf_row32 + ka * 4);
           }
@@ -346,8 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const Tile tc = decode_tile(tile, unit_base, p.E, NT);
       const int row_local = tc.mt * G::kUnitRows + quad * 32 + lane;
       // a 64-row unit fills accumulator lanes 0..63 only: the warps of quadrants 2 and 3 keep
-      // step with the tile hand-off (wait, release) and store nothing
-      const bool lanes_used = G::kUnitRows == kRowTile || quad < 2;
+      // step with the tile hand-off (wait, release) and store nothing; so do the warps of
+      // columns [128, 256) of a 128-column last N tile
+      const bool lanes_used = (G::kUnitRows == kRowTile || quad < 2) && tc.nt * kNTile + half * 128 < p.N;
       const bool valid = lanes_used && row_local < p.counts[tc.e];
       const int64_t prow = (int64_t)tile_base[tc.e] * kRowTile + row_local;
       if (!warp_wait(tmem_full_bar, acc_phase, sync, p.timeout_ns)) break;

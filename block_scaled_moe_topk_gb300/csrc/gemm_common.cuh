@@ -1,6 +1,5 @@
-// gemm_common.cuh -- pieces shared by the grouped GEMM kernels (gemm.cu: one CTA per tile,
-// gemm_pair.cu: CTA pairs): operand-format traits and the instruction descriptor, tile
-// decoding over the experts' M tiles, bounded mbarrier waits, the epilogue stores (SwiGLU +
+// gemm_common.cuh -- pieces of the grouped GEMM kernels: operand-format traits and the
+// instruction descriptor, tile decoding over the experts' M tiles, bounded mbarrier waits, the epilogue stores (SwiGLU +
 // MX requant, or bf16 rows), and the driver entry point that encodes TMA tensor maps.
 #pragma once
 #include <cuda.h>
@@ -37,7 +36,7 @@ struct ActTraits<1> {                  // E2M1 x E2M1, packed
 };
 
 // Block-scaled instruction descriptor: formats, N>>3 at [17,23), E8M0 scales (bit 23),
-// M>>4 at [24,29) (M = 128 for one CTA, 256 for a CTA pair); K-major A and B; scale-factor
+// M>>4 at [24,29) (M = 128, one CTA); K-major A and B; scale-factor
 // byte ids at [29,31) (A) and [4,6) (B).
 template <int ACT>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id, int M) {

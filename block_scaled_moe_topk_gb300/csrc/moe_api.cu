@@ -142,7 +142,7 @@ int launch_count(int64_t T) { return T <= 0 ? 0 : (T <= moe::kSmallRouteTokens ?
 moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits, const uint8_t* w1,
                      const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T, int H,
                      int I, int E, int k, void* ws, size_t ws_bytes, void* stream, moe_act_fmt_t fmt,
-                     bool tiled_scales, cudaEvent_t* ev = nullptr, int gemm_tiles = MOE_GEMM_TILES_AUTO) {
+                     bool tiled_scales, cudaEvent_t* ev = nullptr, int schedule = MOE_SCHEDULE_AUTO) {
   // with T == 0 nothing is read or written, so empty x / logits / out may be null
   if ((T > 0 && (!x || !logits || !out)) || !w1 || !w1s || !w2 || !w2s || !ws) return MOE_ERR_INVALID_ARG;
   moe_workspace_layout_t L;
@@ -152,17 +152,11 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
       !aligned(w1s, tiled_scales ? 16 : 4) || !aligned(w2s, tiled_scales ? 16 : 4) || !aligned(ws, 256))
     return MOE_ERR_MISALIGNED;
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (gemm_tiles != MOE_GEMM_TILES_AUTO && gemm_tiles != MOE_GEMM_TILES_SINGLE && gemm_tiles != MOE_GEMM_TILES_PAIR)
-    return MOE_ERR_INVALID_ARG;
-  if (gemm_tiles == MOE_GEMM_TILES_PAIR && !tiled_scales) return MOE_ERR_INVALID_ARG;
+  if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   DeviceInfo dev;
   st = device_info(&dev);
   if (st != MOE_OK) return st;
-  // single-CTA tiles unless pairs are asked for: on every measured shape (V4-Pro, V4.1-Flash and
-  // draft experts, T = 1 ... 32768) the single-CTA kernel was as fast or faster
-  const bool pair1 = gemm_tiles == MOE_GEMM_TILES_PAIR;
-  const bool pair2 = gemm_tiles == MOE_GEMM_TILES_PAIR;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* W = static_cast<uint8_t*>(ws);
@@ -236,8 +230,7 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
     return few_rows && K / 128 >= moe::kUnit64MinStages ? 64 : kRowTile;
   };
   g1.a_rows = a_rows_for(H);
-  cudaError_t err = pair1 ? moe::launch_gemm_pair(g1, s) : moe::launch_gemm(g1, s);
-  MOE_CUDA_TRY(err);
+  MOE_CUDA_TRY(moe::launch_gemm(g1, s));
   MOE_CUDA_TRY(mark());
 
   moe::GemmArgs g2 = g1;
@@ -248,12 +241,12 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   g2.w_sf = w2s;
   g2.N = H;
   g2.K = I;
-  g2.max_tiles = mtiles_cap * (H / moe::kNTile);
+  g2.max_tiles = mtiles_cap * ((H + moe::kNTile - 1) / moe::kNTile);  // last N tile may be 128 wide
   g2.a_rows = a_rows_for(I);
   g2.out_codes = nullptr;
   g2.out_sf = nullptr;
   g2.out_bf16 = reinterpret_cast<uint16_t*>(at(L.y2));
-  MOE_CUDA_TRY(pair2 ? moe::launch_gemm_pair(g2, s) : moe::launch_gemm(g2, s));
+  MOE_CUDA_TRY(moe::launch_gemm(g2, s));
   MOE_CUDA_TRY(mark());
 
   moe::CombineArgs ca{reinterpret_cast<const uint16_t*>(at(L.y2)), tw, inv_padded, T, H, k, static_cast<uint16_t*>(out)};
@@ -374,7 +367,7 @@ moe_status_t moe_forward_ex(const moe_forward_args_t* a) {
   if (a->prequantized && a->T > 0 && !a->x_scale) return MOE_ERR_INVALID_ARG;
   return forward(a->x, a->prequantized ? a->x_scale : nullptr, a->gate_logits, a->w1, a->w1_scale, a->w2,
                  a->w2_scale, a->out, a->T, a->H, a->I, a->E, a->k, a->workspace, a->workspace_bytes, a->stream,
-                 a->act_fmt, a->weight_scales_prepacked != 0, nullptr, a->gemm_tiles);
+                 a->act_fmt, a->weight_scales_prepacked != 0, nullptr, a->schedule);
 }
 
 moe_status_t moe_a8w4_forward_prequant(const uint8_t* xq, const uint8_t* xq_scale, const float* logits,
@@ -430,7 +423,7 @@ int moe_forward_launch_count(int64_t T) { return launch_count(T); }
 moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* logits, const uint8_t* w1,
                                  const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T,
                                  int H, int I, int E, int k, void* ws, size_t ws_bytes, void* stream,
-                                 int prepacked_scales, int gemm_tiles, float* kernel_us) {
+                                 int prepacked_scales, int schedule, float* kernel_us) {
   if (!kernel_us) return MOE_ERR_INVALID_ARG;
   if (fmt != MOE_ACT_MXFP8 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
   cudaEvent_t ev[kForwardKernels + 1] = {};
@@ -439,7 +432,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* 
     if (cudaEventCreate(&ev[i]) != cudaSuccess) st = MOE_ERR_CUDA;
   if (st == MOE_OK)
     st = forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt,
-                 prepacked_scales != 0, ev, gemm_tiles);
+                 prepacked_scales != 0, ev, schedule);
   const int nk = launch_count(T);
   if (st == MOE_OK && T > 0) {
     if (cudaEventSynchronize(ev[nk]) != cudaSuccess) st = MOE_ERR_CUDA;

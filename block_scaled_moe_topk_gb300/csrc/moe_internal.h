@@ -124,8 +124,6 @@ constexpr int kUnit64MaxRowsPerExpert = 16;
 constexpr int kUnit64MinStages = 16;
 // gemm.cu: one CTA per 128-row x 256-column tile (any weight-scale layout).
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
-// gemm_pair.cu: CTA pairs, 256-row x 256-column tiles (prepacked weight scales only).
-cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t s);
 
 
 // combine.cu

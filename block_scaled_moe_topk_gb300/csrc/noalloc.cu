@@ -4,10 +4,11 @@
 // Its scratch (the per-chunk expert histograms and a status word) lives in one fixed
 // array compiled into the library, so every GPU that loads the library keeps these
 // 4 MiB for the life of the process.  In host code the array's name is only a host-side
-// stand-in; the device address is looked up once per device with cudaGetSymbolAddress
-// (with that device current) and handed to the same histogram / scan / scatter kernels the
+// stand-in; the device address is looked up once per device (and again if that device's
+// context is replaced) with cudaGetSymbolAddress, with that device current, and handed to the same histogram / scan / scatter kernels the
 // workspace version uses.  Every call on a device shares the array: the status word is
 // cleared on each call, the histograms are fully rewritten before they are read.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -23,20 +24,55 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_sort_scratch[kScratchBytes];
 
+// The current context's process-unique id (cuCtxGetId), or 0 when none is current or the
+// driver entry points are unavailable.  The driver is reached through the runtime's entry-point
+// query, so the library still links against the CUDA runtime alone.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 // Device address of g_sort_scratch on the current device (nullptr on failure).  The first
-// call on a device performs the lookup; later calls reuse it.
+// call on a device performs the lookup (which also brings up the device's primary context);
+// later calls reuse it as long as the same context is current.  The cache is keyed on the
+// context's unique id, so after cudaDeviceReset (a new primary context, a new module load) the
+// address is looked up again instead of pointing into the destroyed context.
 void* scratch_on_current_device() {
-  static void* addr[kMaxDevices] = {};
+  struct Entry {
+    unsigned long long ctx_id = 0;
+    void* addr = nullptr;
+  };
+  static Entry cache[kMaxDevices];
   static std::mutex mu;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  Entry& e = cache[dev];
+  const unsigned long long id = current_context_id();
+  if (e.addr == nullptr || id == 0 || id != e.ctx_id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sort_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
+    e.addr = p;
+    e.ctx_id = current_context_id();  // the lookup made the primary context current if none was
   }
-  return addr[dev];
+  return e.addr;
 }
 
 bool is_aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }

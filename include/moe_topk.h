@@ -85,22 +85,18 @@ typedef enum {
 } moe_act_fmt_t;
 
 /*
- * How the grouped GEMMs tile the routed rows (moe_forward_ex, moe_profile_forward).
- *   MOE_GEMM_TILES_SINGLE  one CTA per 128-row x 256-column tile (any weight-scale layout);
- *   MOE_GEMM_TILES_PAIR    a cluster of two CTAs per 256-row x 256-column tile, one
- *                          tcgen05.mma.cta_group::2 for both SMs: half the weight bytes per SM
- *                          and a deeper copy ring, but the same tensor-pipe work per SM per
- *                          stage, and an expert with an odd number of 128-row tiles pays for
- *                          a whole pair.  Needs prepacked weight scales.
- *   MOE_GEMM_TILES_AUTO    single tiles (the faster form on every shape measured so far,
- *                          T = 1 ... 32768); every other entry point uses this rule.
- * The two forms compute the same rows with the same arithmetic (results are bit-identical).
+ * How a forward call schedules its work (moe_forward_ex, moe_profile_forward).
+ *   MOE_SCHEDULE_CHAIN  the kernel chain: routing + sort, quantiser, GEMM1, GEMM2, combine;
+ *                       each GEMM runs one CTA per 128-row x 256-column tile over the whole K.
+ *   MOE_SCHEDULE_AUTO   the library's choice for the shape and T (every named entry point
+ *                       uses this rule).
+ * Every schedule computes the same routing, permutation and quantised activations bit for
+ * bit; outputs agree within the parity tolerance of the layer.
  */
 typedef enum {
-  MOE_GEMM_TILES_AUTO = 0,
-  MOE_GEMM_TILES_SINGLE = 1,
-  MOE_GEMM_TILES_PAIR = 2
-} moe_gemm_tiles_t;
+  MOE_SCHEDULE_AUTO = 0,
+  MOE_SCHEDULE_CHAIN = 1
+} moe_schedule_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(moe_status_t status);
@@ -194,7 +190,9 @@ moe_status_t moe_sort_by_expert(const int32_t* topk_ids, int64_t T, int E, int k
  *   (with E = 384 that allows T up to 87,360 tokens).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before any
- *   stream capture.  The call allocates nothing.
+ *   stream capture.  The address is cached per device and context: after
+ *   cudaDeviceReset the next call looks it up again (again outside any capture).
+ *   The call allocates nothing.
  *   Every call on a device shares the array: two calls whose kernels overlap on the
  *   GPU (different streams, or several host threads) race on it and must be
  *   serialised by the caller.  Ids outside [0, E) are skipped as in
@@ -312,8 +310,7 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   void* stream;
-  int gemm_tiles;               /* moe_gemm_tiles_t; MOE_GEMM_TILES_PAIR without prepacked
-                                   weight scales is MOE_ERR_INVALID_ARG */
+  int schedule;                 /* moe_schedule_t; any other value is MOE_ERR_INVALID_ARG */
 } moe_forward_args_t;
 moe_status_t moe_forward_ex(const moe_forward_args_t* args);
 
@@ -332,8 +329,8 @@ int moe_forward_launch_count(int64_t T);
 /*
  * Profiling form of the forward: enqueues exactly the launch sequence of
  * moe_a8w4_forward (fmt = MOE_ACT_MXFP8) or moe_a4w4_forward (MOE_ACT_MXFP4),
- * or of their *_prepacked forms when prepacked_scales != 0, with the GEMM
- * tiling gemm_tiles (moe_gemm_tiles_t, as in moe_forward_ex),
+ * or of their *_prepacked forms when prepacked_scales != 0, under the
+ * schedule `schedule` (moe_schedule_t, as in moe_forward_ex),
  * with a CUDA event recorded before the first kernel and after each kernel,
  * waits for the last event, and writes the duration of each kernel in
  * microseconds to kernel_us[moe_forward_launch_count(T)] (HOST array), in
@@ -346,7 +343,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x_bf16, const fl
                                  const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
                                  const uint8_t* w2_scale, void* out_bf16, int64_t T, int H, int I, int E,
                                  int k, void* workspace, size_t workspace_bytes, void* stream,
-                                 int prepacked_scales, int gemm_tiles, float* kernel_us);
+                                 int prepacked_scales, int schedule, float* kernel_us);
 
 #ifdef __cplusplus
 }

@@ -46,6 +46,18 @@ class Weights:
         else:
             self.dev = synth.weights_codes(E, H, I, seed, device=device)
             self.host = tuple(t.cpu().numpy() for t in self.dev)
+        self._prepacked = None
+
+    def dev_prepacked(self):
+        """The device weights with both scale tensors in the library's prepacked tile layout."""
+        if self._prepacked is None:
+            import block_scaled_moe_topk_gb300 as moe
+            w1, w1s, w2, w2s = self.dev
+            t1, t2 = torch.empty_like(w1s), torch.empty_like(w2s)
+            moe.moe_prepack_scales(w1s, t1)
+            moe.moe_prepack_scales(w2s, t2)
+            self._prepacked = (w1, t1, w2, t2)
+        return self._prepacked
 
 
 def compare(got_bits, want_bits):

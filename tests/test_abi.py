@@ -104,14 +104,12 @@ def test_forward_launch_count():
     assert moe.moe_forward_launch_count(65) == 7
 
 
-def test_forward_ex_gemm_tiles_validation():
-    """CTA-pair tiles need prepacked weight scales; an unknown tiling value is rejected.  Both
-    fail host-side validation, before any CUDA call."""
+def test_forward_ex_schedule_validation():
+    """An unknown schedule value is rejected by host-side validation, before any CUDA call."""
     ok = (1 << 20)
     a = moe.ForwardArgs(act_fmt=0, prequantized=0, weight_scales_prepacked=0, x=ok, x_scale=None, gate_logits=ok,
                         w1=ok, w1_scale=ok, w2=ok, w2_scale=ok, out=ok, T=16, H=256, I=128, E=8, k=2, workspace=ok,
-                        workspace_bytes=1 << 30, stream=None, gemm_tiles=moe.MOE_GEMM_TILES_PAIR)
+                        workspace_bytes=1 << 30, stream=None, schedule=7)
     assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 1
-    a.weight_scales_prepacked = 1
-    a.gemm_tiles = 7
+    a.schedule = -1
     assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 1

@@ -134,13 +134,39 @@ def test_quant_bit_exact(fmt, rows, K):
 
 
 # --------------------------------------------------------------------------- forward
-def _run_forward(act, x, lg, W, E, k):
+# Entry points of the forward, each compared with the oracle on the same inputs:
+#   bf16       moe_a8w4_forward / moe_a4w4_forward (canonical weight scales)
+#   prepacked  moe_a8w4_forward_prepacked / moe_a4w4_forward_prepacked
+#   prequant   moe_a8w4_forward_prequant / moe_a4w4_forward_prequant, fed the ORACLE's codes of x
+#   ex         moe_forward_ex with the oracle's codes of x and prepacked weight scales
+ENTRIES = ("bf16", "prepacked", "prequant", "ex")
+
+
+def _run_forward(act, x, lg, W, E, k, entry="bf16", schedule=None):
     T, H = x.shape
     I = W.I
     out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
     ws = torch.empty(moe.moe_workspace_bytes(T, H, I, E, k, act), dtype=torch.uint8, device=DEV)
-    f = moe.moe_a8w4_forward if act == moe.MOE_ACT_MXFP8 else moe.moe_a4w4_forward
-    f(x.to(DEV), lg.to(DEV), *W.dev, out, E, k, ws)
+    xd, lgd = x.to(DEV), lg.to(DEV)
+    a8 = act == moe.MOE_ACT_MXFP8
+    if entry == "bf16" and schedule is None:
+        (moe.moe_a8w4_forward if a8 else moe.moe_a4w4_forward)(xd, lgd, *W.dev, out, E, k, ws)
+    elif entry == "bf16":
+        moe.moe_forward_ex(xd, lgd, *W.dev, out, E, k, ws, act_fmt=act, schedule=schedule)
+    elif entry == "prepacked":
+        f = moe.moe_a8w4_forward_prepacked if a8 else moe.moe_a4w4_forward_prepacked
+        f(xd, lgd, *W.dev_prepacked(), out, E, k, ws)
+    else:
+        # the oracle's own codes of x: no input of this path comes from the CUDA quantiser
+        xq_h, xs_h = oracle.quantize_rows_bf16(synth.bf16_bits(x), act)
+        xq, xs = torch.from_numpy(xq_h).to(DEV), torch.from_numpy(xs_h).to(DEV)
+        if entry == "prequant":
+            f = moe.moe_a8w4_forward_prequant if a8 else moe.moe_a4w4_forward_prequant
+            f(xq, xs, lgd, *W.dev, out, E, k, ws)
+        else:
+            moe.moe_forward_ex(xq, lgd, *W.dev_prepacked(), out, E, k, ws, act_fmt=act, x_scale=xs,
+                               weight_scales_prepacked=True,
+                               schedule=moe.MOE_SCHEDULE_AUTO if schedule is None else schedule)
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0
     return out, ws
@@ -210,8 +236,9 @@ def test_forward_tiny_full(act):
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
 
 
-@pytest.mark.parametrize("T", [1, 2, 8, 64])
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16, 32, 64])
 def test_forward_flash_decode(T):
+    """Every token count of the V4.1-Flash decode config, each whole batch against the oracle."""
     s = synth.SHAPES["flash_decode"]
     W = _weights(s)
     x, lg = synth.x_bf16(T, s.H, 0), synth.gate_logits(T, s.E, 0)
@@ -234,13 +261,14 @@ def _weights(s):
     return _WCACHE[key]
 
 
-def _sampled_check(act, s, T, n_sample, seed=0):
+def _sampled_check(act, s, T, n_sample, seed=0, entry="bf16", schedule=None):
+    """The forward at full size; the oracle on a seeded sample of its tokens plus every token
+    (up to 32) of the most- and least-loaded active experts."""
     W = _weights(s)
     x, lg = synth.x_bf16(T, s.H, seed), synth.gate_logits(T, s.E, seed, skew=s.skew)
-    out, ws = _run_forward(act, x, lg, W, s.E, s.k)
+    out, ws = _run_forward(act, x, lg, W, s.E, s.k, entry=entry, schedule=schedule)
     rng = np.random.default_rng(T)
     toks = np.sort(rng.choice(T, size=min(n_sample, T), replace=False))
-    # add every token of the most- and least-loaded active expert (bounded)
     ids_h, _ = oracle.route(lg.numpy(), s.k)
     cnt = np.bincount(ids_h.reshape(-1), minlength=s.E)
     for e in (int(cnt.argmax()), int(np.where(cnt > 0, cnt, cnt.max() + 1).argmin())):
@@ -252,9 +280,14 @@ def _sampled_check(act, s, T, n_sample, seed=0):
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
 
 
-@pytest.mark.parametrize("T", [1, 64, 77, 3072])
+@pytest.mark.parametrize("T", [1, 16, 64, 77, 1024, 3072])
 def test_forward_draft_skewed(T):
     _sampled_check(moe.MOE_ACT_MXFP8, synth.SHAPES["draft"], T, 48)
+
+
+@pytest.mark.slow
+def test_forward_draft_skewed_24576():
+    _sampled_check(moe.MOE_ACT_MXFP8, synth.SHAPES["draft"], 24576, 48)
 
 
 @pytest.mark.slow
@@ -265,9 +298,36 @@ def test_forward_pro_a8w4(T, skew):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("T", [512])
+@pytest.mark.parametrize("T", [512, 1024, 8192])
 def test_forward_pro_a4w4(T):
     _sampled_check(moe.MOE_ACT_MXFP4, synth.SHAPES["pro"], T, 24)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("entry", ["prepacked", "prequant", "ex"])
+def test_forward_pro_entry_points(entry, act):
+    """The V4-Pro layer at T = 8192 (the benchmarked size; the A8W4 prepacked form is the exact
+    benchmarked call) through every other entry point, against the oracle."""
+    _sampled_check(act, synth.SHAPES["pro"], 8192, 16, entry=entry)
+
+
+@pytest.mark.parametrize("entry", ENTRIES)
+@pytest.mark.parametrize("shape,T,act", [("tiny", 16, moe.MOE_ACT_MXFP8), ("tiny", 16, moe.MOE_ACT_MXFP4),
+                                         ("flash_decode", 100, moe.MOE_ACT_MXFP8),
+                                         ("flash_decode", 5, moe.MOE_ACT_MXFP4),
+                                         ("draft", 300, moe.MOE_ACT_MXFP4)])
+def test_forward_entry_points_against_oracle(entry, shape, T, act):
+    """Every entry point against the oracle on the whole batch (tiny weights are bf16 draws
+    quantised by the oracle; the others MXFP4 codes drawn directly)."""
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 4), synth.gate_logits(T, s.E, 4, skew=s.skew)
+    out, ws = _run_forward(act, x, lg, W, s.E, s.k, entry=entry)
+    _check_intermediates(act, x, lg, W, s.E, s.k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, act)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
 
 
 # --------------------------------------------------------------------------- properties
@@ -429,7 +489,7 @@ def test_forward_64_row_units_with_a_crowded_expert():
 
 def test_forward_independent_of_stale_workspace():
     """The padding rows of the expert segments are never written: a workspace full of stale
-    random bytes gives the zeroed workspace's output bit for bit (both formats, both tilings)."""
+    random bytes gives the zeroed workspace's output bit for bit (both formats)."""
     s = synth.SHAPES["flash_decode"]
     W = _weights(s)
     T = 300
@@ -441,47 +501,38 @@ def test_forward_independent_of_stale_workspace():
         nbytes = moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act)
         outs = []
         for fill in ("zeros", "random"):
-            for tiles in (moe.MOE_GEMM_TILES_SINGLE, moe.MOE_GEMM_TILES_PAIR):
-                ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
-                if fill == "random":
-                    ws.random_(0, 256, generator=gen)
-                out = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
-                moe.moe_forward_ex(x, lg, *Wp, out, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=True,
-                                   gemm_tiles=tiles)
-                torch.cuda.synchronize()
-                assert moe.moe_read_device_status(ws) == 0
-                outs.append(out)
-        for o in outs[1:]:
-            assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+            if fill == "random":
+                ws.random_(0, 256, generator=gen)
+            out = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+            moe.moe_forward_ex(x, lg, *Wp, out, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=True)
+            torch.cuda.synchronize()
+            assert moe.moe_read_device_status(ws) == 0
+            outs.append(out)
+        assert torch.equal(outs[1].view(torch.int16), outs[0].view(torch.int16))
 
 
-# --------------------------------------------------------------------------- CTA-pair tiles
-@pytest.mark.parametrize("shape,T,act", [("tiny", 16, moe.MOE_ACT_MXFP8), ("tiny", 16, moe.MOE_ACT_MXFP4),
-                                         ("flash_decode", 300, moe.MOE_ACT_MXFP8), ("draft", 3072, moe.MOE_ACT_MXFP8),
-                                         ("draft_tp4", 2000, moe.MOE_ACT_MXFP4), ("pro", 1024, moe.MOE_ACT_MXFP4),
-                                         ("pro", 4096, moe.MOE_ACT_MXFP8)])
-def test_forward_pair_tiles_are_bit_identical(shape, T, act):
-    """256-row tiles on CTA pairs (tcgen05 cta_group::2) give the single-CTA tiles' output bit for
-    bit: both GEMMs, experts with odd and even tile counts (odd ones leave the second CTA of
-    their last pair without rows), and A4W4's ragged last K stage (I = 640)."""
-    s = synth.SHAPES[shape]
-    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
-    x, lg = synth.x_bf16(T, s.H, 6).to(DEV), synth.gate_logits(T, s.E, 6, skew=s.skew).to(DEV)
+# --------------------------------------------------------------------------- TP-shard shapes
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("H,I,T", [(384, 128, 16), (640, 384, 200), (384, 128, 1)])
+def test_forward_hidden_size_not_a_multiple_of_256(act, H, I, T):
+    """GEMM2 tiles its H output columns 256 at a time; an H that is an odd multiple of 128 ends
+    in a 128-column tile, whose columns must all be computed (the combine reads every one)."""
+    E, k = 8, 2
+    W = Weights(E, H, I, seed=1, device=DEV, from_bf16=True)
+    x, lg = synth.x_bf16(T, H, 3), synth.gate_logits(T, E, 3)
+    out, ws = _run_forward(act, x, lg, W, E, k)
+    _check_intermediates(act, x, lg, W, E, k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, act)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+    # the prepacked weight-scale path reads the same columns
     w1, w1s, w2, w2s = W.dev
-    Wp = (w1, _prepack(w1s), w2, _prepack(w2s))
-    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act), dtype=torch.uint8, device=DEV)
-    outs = []
-    for tiles in (moe.MOE_GEMM_TILES_SINGLE, moe.MOE_GEMM_TILES_PAIR):
-        out = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
-        moe.moe_forward_ex(x, lg, *Wp, out, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=True, gemm_tiles=tiles)
-        torch.cuda.synchronize()
-        assert moe.moe_read_device_status(ws) == 0
-        outs.append(out)
-    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
-    if shape == "tiny":
-        want = oracle.moe_forward(synth.bf16_bits(x.cpu()), lg.cpu().numpy(), *W.host, s.E, s.k, act)
-        rel, cos = compare(bits(outs[1]), want)
-        assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+    out_p = torch.empty_like(out)
+    moe.moe_forward_ex(x.to(DEV), lg.to(DEV), w1, _prepack(w1s), w2, _prepack(w2s), out_p, E, k, ws, act_fmt=act,
+                       weight_scales_prepacked=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p.view(torch.int16), out.view(torch.int16))
 
 
 @pytest.mark.parametrize("shape,T", [("flash_tp2", 1), ("flash_tp2", 96), ("draft_tp4", 3), ("draft_tp4", 500)])

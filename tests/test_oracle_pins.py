@@ -178,6 +178,36 @@ def test_quantize_rows_matches_independent_reference(fmt):
     assert np.array_equal(np.signbit(got_vals), np.signbit(want_vals))
 
 
+@pytest.mark.parametrize("fmt", [E4M3, E2M1])
+def test_dequantize_rows_against_torch_and_tables(fmt):
+    """Row decoder: every code (E4M3 through torch's float8_e4m3fn, E2M1 through the literal
+    table with element 2i in the low nibble) times 2^(s - 127) of its 32-block's scale byte."""
+    rng = np.random.default_rng(17)
+    rows, K = 5, 256
+    if fmt == E4M3:
+        codes = rng.integers(0, 256, (rows, K), dtype=np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes: the quantiser never emits them
+        elem = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    else:
+        codes = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+        table = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                          -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+        elem = np.empty((rows, K))
+        elem[:, 0::2] = table[codes & 15]
+        elem[:, 1::2] = table[codes >> 4]
+    scales = rng.integers(0, 255, (rows, K // 32), dtype=np.uint8)
+    scales[0, 0], scales[1, 1] = 0, 254  # the extreme finite scales
+    got = oracle.dequantize_rows(codes, scales, K, fmt)
+    want = elem * np.ldexp(1.0, np.repeat(scales.astype(int), 32, axis=1) - 127)
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+    # and it inverts the row quantiser on values that lie on the MX grid
+    v = (elem[:2] * 2.0 ** -3).astype(np.float32)
+    c, sc = oracle.quantize_rows_f32(v, fmt)
+    back = oracle.dequantize_rows(c, sc, K, fmt)
+    assert np.array_equal(back, v.astype(np.float64))
+
+
 def test_bf16_rows_and_nibble_order():
     """bf16 entry point equals the fp32 one; FP4 element 2i sits in the low nibble."""
     x = synth.x_bf16(4, 128, seed=11)
