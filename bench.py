@@ -177,13 +177,34 @@ def measured_traffic():
     return d.get("bytes_per_headline_launch") if d.get("gemm_sources_sha256") == gemm_sources_sha() else None
 
 
-def gemm1_algorithmic(T, active):
-    """GEMM1 bytes: active experts' W1 codes + scales, the routed activation rows and their
-    scales read, the A2 rows and scales written; flops 2 * R * 2I * H."""
+def pct_us(reps_ms):
+    """p10 / p90 of a list of per-replay milliseconds, in microseconds."""
+    return {"p10_us": round(float(np.percentile(reps_ms, 10)) * 1e3, 2),
+            "p90_us": round(float(np.percentile(reps_ms, 90)) * 1e3, 2), "replays": len(reps_ms)}
+
+
+def gemm_algorithmic(T, active, which):
+    """Algorithmic bytes and flops of one GEMM launch: the active experts' canonical weight codes
+    + E8M0 scales (W1 for GEMM1, W2 for GEMM2) and 2 * R * N * K flops over the routed rows.
+    The quantised activations, A2 and y2 are intermediates, not algorithmic bytes."""
     R = T * SHAPE.k
-    B = active * W1_BYTES + R * (SHAPE.H + SHAPE.H // 32) + R * (SHAPE.I + SHAPE.I // 32)
-    F = 2 * R * 2 * SHAPE.I * SHAPE.H
-    return B, F
+    if which == 1:
+        return active * W1_BYTES, 2 * R * 2 * SHAPE.I * SHAPE.H
+    return active * W2_BYTES, 2 * R * SHAPE.H * SHAPE.I
+
+
+def kernel_roofline(name, B, F, us, pk):
+    """Roofline entry of one kernel from its algorithmic bytes/flops and measured duration."""
+    t_bytes, t_flops = B / (pk["hbm"] * 1e9), F / (2.0 * pk["bf16"] * 1e12)
+    sec = us * 1e-6
+    if t_bytes >= t_flops:
+        achieved, peak, unit, bound = B / sec / 1e9, pk["hbm"], "GB/s", "hbm"
+    else:
+        achieved, peak, unit, bound = F / sec / 1e12, 2.0 * pk["bf16"], "TFLOP/s", "tensor"
+    return {"kernel": name, "bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "us": round(us, 2), "algorithmic_bytes": B, "algorithmic_flops": F,
+            "tensor_frac": round(F / sec / (2.0 * pk["bf16"] * 1e12), 4),
+            "peak_source": pk["source"] + (" (MXFP8 = 2 x measured bf16)" if bound == "tensor" else " copy")}
 
 
 def run_ours(args):
@@ -274,18 +295,9 @@ def run_ours(args):
         flush.fill_(1)
         prof.append(moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W, out, E, k, ws, prepacked_scales=True))
     kern_us = {n: statistics.mean(p[n] for p in prof[1:]) for n in prof[0]}
-    g1_bytes, g1_flops = gemm1_algorithmic(T, active)
-    g1_s = kern_us["gemm1"] * 1e-6
-    t_bytes, t_flops = g1_bytes / (pk["hbm"] * 1e9), g1_flops / (2.0 * pk["bf16"] * 1e12)
-    if t_bytes >= t_flops:
-        achieved, peak, unit, bound = g1_bytes / g1_s / 1e9, pk["hbm"], "GB/s", "hbm"
-    else:
-        achieved, peak, unit, bound = g1_flops / g1_s / 1e12, 2.0 * pk["bf16"], "TFLOP/s", "tensor"
-    roofline = {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
-                "frac": round(achieved / peak, 4),
-                "traffic": args.traffic if args.traffic is not None else measured_traffic(), "kernel": "gemm1",
-                "peak_source": pk["source"] + (" (MXFP8 = 2 x measured bf16)" if bound == "tensor" else ""),
-                "algorithmic_bytes": g1_bytes, "algorithmic_flops": g1_flops}
+    roofline = kernel_roofline("gemm1", *gemm_algorithmic(T, active, 1), kern_us["gemm1"], pk)
+    roofline["traffic"] = args.traffic if args.traffic is not None else measured_traffic()
+    roofline["gemm2"] = kernel_roofline("gemm2", *gemm_algorithmic(T, active, 2), kern_us["gemm2"], pk)
 
     # ---------------------------------------------------------------- end to end, host buffers
     # Every step copies its inputs from pinned host memory, runs the forward through the C ABI
@@ -363,13 +375,15 @@ def run_ours(args):
         xs_, lgs_ = make_workload(t_, rank, dev, E)
         o_ = torch.empty(t_, H, dtype=torch.bfloat16, device=dev)
         g_ = graph_for(xs_, lgs_, o_)
-        ms = statistics.median(timed_replays(g_, max(5, min(args.steps, 30)), 3))
+        reps = timed_replays(g_, args.sweep_replays, 3)
+        ms = statistics.median(reps)
         act = active_experts()
         B, F, th, tt = layer_roofline(t_, act, pk, E)
-        rows.append({"T": t_, "us": round(ms * 1e3, 2), "tok_s": round(t_ / (ms / 1e3), 1),
+        rows.append({"T": t_, "us": round(ms * 1e3, 2), **pct_us(reps), "tok_s": round(t_ / (ms / 1e3), 1),
                      "routed_rows_s": round(t_ * k / (ms / 1e3), 1), "active_experts": act,
                      "bytes": B, "flops": F, "bound": "hbm" if th >= tt else "tensor",
-                     "roofline_us": round(max(th, tt) * 1e6, 2), "frac": round(max(th, tt) / (ms / 1e3), 4)})
+                     "roofline_us": round(max(th, tt) * 1e6, 2), "frac": round(max(th, tt) / (ms / 1e3), 4),
+                     "hbm_frac": round(th / (ms / 1e3), 4), "tensor_frac": round(tt / (ms / 1e3), 4)})
         del g_
 
     def point(f, weights, x_, lg_, E_, k_, H_, I_, ws_, fmt=moe.MOE_ACT_MXFP8):
@@ -379,19 +393,19 @@ def run_ours(args):
         g_ = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_):
             f(x_, lg_, *weights, o_, E_, k_, ws_, stream=torch.cuda.current_stream())
-        ms_ = statistics.median(timed_replays(g_, 5, 3))
+        reps = timed_replays(g_, args.sweep_replays, 3)
         act_ = int((moe.workspace_views(ws_, x_.shape[0], H_, I_, E_, k_, fmt)["counts"] > 0).sum().item())
         del g_
-        return ms_, act_
+        return statistics.median(reps), act_, pct_us(reps)
 
     # ---------------------------------------------------------------- A4W4 (same weights)
     a4 = []
     if not args.quick_extras:
         for t_ in (512, 1024, 8192):
             xs_, lgs_ = make_workload(t_, rank, dev, E)
-            ms_, act_ = point(moe.moe_a4w4_forward_prepacked, W, xs_, lgs_, E, k, H, I, ws, moe.MOE_ACT_MXFP4)
+            ms_, act_, pc_ = point(moe.moe_a4w4_forward_prepacked, W, xs_, lgs_, E, k, H, I, ws, moe.MOE_ACT_MXFP4)
             B_, F_, th_, tt_ = shape_roofline(t_, act_, pk, H, I, E, k, fp4_act=True)
-            a4.append({"T": t_, "us": round(ms_ * 1e3, 2), "tok_s": round(t_ / (ms_ / 1e3), 1),
+            a4.append({"T": t_, "us": round(ms_ * 1e3, 2), **pc_, "tok_s": round(t_ / (ms_ / 1e3), 1),
                        "bound": "hbm" if th_ >= tt_ else "tensor", "roofline_us": round(max(th_, tt_) * 1e6, 2),
                        "frac": round(max(th_, tt_) / (ms_ / 1e3), 4)})
 
@@ -403,7 +417,7 @@ def run_ours(args):
     def prequant_fwd(x_, lg_, w1, w1s, w2, w2s, o_, E_, k_, ws_, stream=None):
         moe.moe_forward_ex(xq_, lg_, w1, w1s, w2, w2s, o_, E_, k_, ws_, x_scale=xsc_, weight_scales_prepacked=True,
                            stream=stream)
-    pre_ms, _ = point(prequant_fwd, W, x, lg, E, k, H, I, ws)
+    pre_ms, _, _ = point(prequant_fwd, W, x, lg, E, k, H, I, ws)
 
     # ---------------------------------------------------------------- the other layer shapes of the configs
     cfg = {}
@@ -425,9 +439,9 @@ def run_ours(args):
             for t_ in Ts:
                 xs_ = synth.x_bf16(t_, sh.H, seed=rank, device=dev)
                 lgs_ = synth.gate_logits(t_, sh.E, seed=rank, skew=sh.skew, device=dev)
-                ms_, act_ = point(fwd, Wsh, xs_, lgs_, sh.E, sh.k, sh.H, sh.I, ws_sh)
+                ms_, act_, pc_ = point(fwd, Wsh, xs_, lgs_, sh.E, sh.k, sh.H, sh.I, ws_sh)
                 B_, F_, th_, tt_ = shape_roofline(t_, act_, pk, sh.H, sh.I, sh.E, sh.k)
-                rows_sh.append({"T": t_, "us": round(ms_ * 1e3, 2), "active_experts": act_,
+                rows_sh.append({"T": t_, "us": round(ms_ * 1e3, 2), **pc_, "active_experts": act_,
                                 "frac": round(max(th_, tt_) / (ms_ / 1e3), 4)})
             cfg[f"{name} H={sh.H} I={sh.I} E={sh.E} k={sh.k}{' skewed' if sh.skew else ''}"] = rows_sh
             del Wsc, Wsh, t1, t2, ws_sh
@@ -437,7 +451,7 @@ def run_ours(args):
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(x, lg, W, args.cpu_tokens, E)
+        cpu = cpu_baseline(x, lg, Wc, args, E)
 
     B, F, th, tt = layer_roofline(T, active, pk, E)
     line = {
@@ -461,7 +475,9 @@ def run_ours(args):
         "a4w4": a4, "config_sweeps": cfg,
         "layer_roofline": {"bytes": B, "flops": F, "active_experts": active, "t_hbm_us": round(th * 1e6, 2),
                            "t_tensor_us": round(tt * 1e6, 2), "bound": "hbm" if th >= tt else "tensor",
-                           "frac": round(max(th, tt) / (ms_per_step / 1e3), 4), "peaks": pk["source"]},
+                           "frac": round(max(th, tt) / (ms_per_step / 1e3), 4),
+                       "hbm_frac": round(th / (ms_per_step / 1e3), 4),
+                       "tensor_frac": round(tt / (ms_per_step / 1e3), 4), "peaks": pk["source"]},
         "roofline": roofline, "kernel_us": {n: round(v, 2) for n, v in kern_us.items()},
         "e2e": e2e, "gpu_launches": args.steps * moe.moe_forward_launch_count(T),
         "device_status": status, "sweep": rows, "clocks": clk, "cpu_baseline": cpu,
@@ -473,24 +489,79 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(x, lg, W, n_tokens, E):
-    """The oracle as it stands, on all host cores, on the first n_tokens tokens of the batch."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _time_oracle(xb, lgh, host_w, E, k, nthreads, fmt):
     import oracle
-    host_w = [w.cpu().numpy() for w in W]
-    xb = synth.bf16_bits(x[:n_tokens])
-    lgh = lg[:n_tokens].cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.moe_forward(xb, lgh, *host_w, E, k, fmt, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(x, lg, Wc, args, E):
+    """The oracle as it stands, timed on the host cores (single thread and all cores), on the
+    plan of the measurement protocol: every token count of the tiny and V4.1-Flash decode
+    configs and of the V4-Pro config up to T = 1024 run in full; above that a seeded sample of
+    the batch is timed and scaled to T (marked extrapolated)."""
+    import oracle
     cores = oracle.max_threads()
-    t0 = time.perf_counter()
-    oracle.moe_forward(xb, lgh, *host_w, E, SHAPE.k, oracle.FMT_E4M3, nthreads=cores)
-    dt = time.perf_counter() - t0
-    n1 = max(1, n_tokens // 8)  # the same oracle on one core, on a smaller sample
-    t0 = time.perf_counter()
-    oracle.moe_forward(xb[:n1], lgh[:n1], *host_w, E, SHAPE.k, oracle.FMT_E4M3, nthreads=1)
-    dt1 = time.perf_counter() - t0
-    return {"value": round(n_tokens / dt, 3), "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n_tokens} tokens of the same batch, whole layer per token (route, quant, GEMM1, "
-                      f"SwiGLU, A2, GEMM2, combine), fp64 accumulation; {dt:.1f} s wall",
-            "single_core": {"value": round(n1 / dt1, 3), "unit": "tok/s", "sample": f"{n1} tokens, {dt1:.1f} s wall"}}
+    host_w = [w.cpu().numpy() for w in Wc]  # canonical scales: what the oracle reads
+    fmt = oracle.FMT_E4M3
+    plan = []
+    # V4-Pro: the headline batch's first n tokens stand for a batch of n tokens
+    xb_all = synth.bf16_bits(x[:max(args.cpu_tokens, 1024)])
+    lg_all = lg[:max(args.cpu_tokens, 1024)].cpu().numpy()
+    for t_ in (1, 16, 128, 512, 1024):
+        if t_ > args.cpu_full_max:
+            continue
+        dt = _time_oracle(xb_all[:t_], lg_all[:t_], host_w, E, SHAPE.k, cores, fmt)
+        plan.append({"config": "pro", "T": t_, "seconds": round(dt, 3), "tok_s": round(t_ / dt, 3),
+                     "threads": cores, "kind": "full"})
+    n = args.cpu_tokens
+    dt = _time_oracle(xb_all[:n], lg_all[:n], host_w, E, SHAPE.k, cores, fmt)
+    per_tok = dt / n
+    for t_ in (4096, 8192, 16384, 32768):
+        plan.append({"config": "pro", "T": t_, "seconds": round(per_tok * t_, 1), "tok_s": round(1 / per_tok, 3),
+                     "threads": cores, "kind": f"extrapolated from {n} tokens"})
+    n1 = args.cpu_single_tokens
+    dt1 = _time_oracle(xb_all[:n1], lg_all[:n1], host_w, E, SHAPE.k, 1, fmt)
+    del host_w
+    # the tiny and V4.1-Flash decode configs, every token count, whole batches
+    for name, Ts in (("tiny", [16]), ("flash_decode", [1, 2, 4, 8, 16, 32, 64])):
+        sh = synth.SHAPES[name]
+        Wh = [w.cpu().numpy() for w in synth.weights_codes(sh.E, sh.H, sh.I, seed=0, device=x.device)]
+        for t_ in Ts:
+            xs_ = synth.bf16_bits(synth.x_bf16(t_, sh.H, seed=0))
+            lgs_ = synth.gate_logits(t_, sh.E, seed=0).numpy()
+            for th in (cores, 1):
+                d = _time_oracle(xs_, lgs_, Wh, sh.E, sh.k, th, fmt)
+                plan.append({"config": name, "T": t_, "seconds": round(d, 4), "tok_s": round(t_ / d, 3),
+                             "threads": th, "kind": "full"})
+    return {"value": round(n / dt, 3), "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"{n} tokens of the V4-Pro T={x.shape[0]} batch, whole layer per token (route, quant, GEMM1, "
+                      f"SwiGLU, A2, GEMM2, combine), fp64 accumulation; {dt:.1f} s wall on {cores} threads; "
+                      f"the batch's time is extrapolated ({per_tok * x.shape[0]:.0f} s for T={x.shape[0]})",
+            "single_core": {"value": round(n1 / dt1, 3), "unit": "tok/s", "threads": 1,
+                            "sample": f"{n1} tokens, {dt1:.1f} s wall"},
+            "plan": plan}
 
 
 def run_reference(args):
@@ -546,7 +617,11 @@ def main():
     ap.add_argument("--quick-extras", action="store_true", help="skip the A4W4 and per-config sweeps")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--cpu-tokens", type=int, default=256, help="V4-Pro tokens of the all-core oracle sample")
+    ap.add_argument("--cpu-single-tokens", type=int, default=16, help="V4-Pro tokens of the one-thread sample")
+    ap.add_argument("--cpu-full-max", type=int, default=1024,
+                    help="largest V4-Pro token count the oracle runs in full (the protocol's 1024)")
+    ap.add_argument("--sweep-replays", type=int, default=50, help="graph replays per sweep point")
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMM1 launch from an ncu capture of the current kernel")
