@@ -14,11 +14,12 @@ import os
 import torch
 
 __all__ = [
-    "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "MOE_SCHEDULE_AUTO", "MOE_SCHEDULE_CHAIN", "lib", "moe_status_string", "moe_workspace_bytes",
+    "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "MOE_SCHEDULE_AUTO", "MOE_SCHEDULE_CHAIN", "MOE_SCHEDULE_FUSED",
+    "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
     "moe_quantize_mx", "moe_a8w4_forward",
     "moe_a4w4_forward", "moe_forward_ex", "moe_a8w4_forward_prequant", "moe_a4w4_forward_prequant", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
-    "moe_read_device_status", "moe_forward_launch_count", "moe_profile_forward",
+    "moe_read_device_status", "moe_forward_launch_count", "moe_forward_launch_count_ex", "moe_profile_forward",
     "workspace_views",
 ]
 
@@ -26,6 +27,7 @@ MOE_ACT_MXFP8 = 0
 MOE_ACT_MXFP4 = 1
 MOE_SCHEDULE_AUTO = 0   # the library's choice for the shape and T
 MOE_SCHEDULE_CHAIN = 1  # kernel chain, one CTA per 128 x 256 GEMM tile over the whole K
+MOE_SCHEDULE_FUSED = 2  # T <= 64: the whole layer in one persistent kernel
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_topk.so")
 
 STATUS_NAMES = {
@@ -42,8 +44,8 @@ class MoeError(RuntimeError):
 
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "status", "topk_ids", "topk_w", "counts", "offsets", "padded_offsets", "mtile_base", "chunk_hist",
-        "sorted_pair", "inv", "inv_padded", "xq", "xs", "a2", "a2s", "y2", "total")] + [
+        "status", "sync", "topk_ids", "topk_w", "counts", "offsets", "padded_offsets", "mtile_base", "chunk_hist",
+        "sorted_pair", "inv", "inv_padded", "xq", "xs", "a2", "a2s", "y2", "part", "y2f", "total")] + [
         ("rows_cap", ctypes.c_int64), ("nchunk", ctypes.c_int64)]
 
 
@@ -90,6 +92,8 @@ def lib():
     L.moe_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
     L.moe_forward_launch_count.restype = i32
     L.moe_forward_launch_count.argtypes = [i64]
+    L.moe_forward_launch_count_ex.restype = i32
+    L.moe_forward_launch_count_ex.argtypes = [i64, i32]
     L.moe_profile_forward.restype = i32
     L.moe_profile_forward.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P, i32, i32,
                                       ctypes.POINTER(ctypes.c_float)]
@@ -139,6 +143,10 @@ def moe_workspace_bytes(T, H, I, E, k, fmt=MOE_ACT_MXFP8) -> int:
 
 def moe_forward_launch_count(T) -> int:
     return int(lib().moe_forward_launch_count(int(T)))
+
+
+def moe_forward_launch_count_ex(T, schedule) -> int:
+    return int(lib().moe_forward_launch_count_ex(int(T), int(schedule)))
 
 
 def moe_topk_route(gate_logits, k, topk_ids, topk_w, stream=None):
@@ -249,7 +257,8 @@ def moe_a4w4_forward_prepacked(x, gate_logits, w1, w1_scale_tiled, w2, w2_scale_
 
 
 KERNEL_NAMES = ("route", "scan", "scatter", "quant", "gemm1", "gemm2", "combine")
-KERNEL_NAMES_SMALL = ("route_sort", "quant", "gemm1", "gemm2", "combine")  # T <= 64
+KERNEL_NAMES_SMALL = ("route_sort", "quant", "gemm1", "gemm2", "combine")  # kernel chain, T <= 64
+KERNEL_NAMES_FUSED = ("decode",)  # fused schedule
 
 
 def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None,
@@ -257,14 +266,15 @@ def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E,
     """One forward with a CUDA event between kernels; returns {kernel name: microseconds}."""
     T, H = x.shape
     I = w2.shape[-1] * 2
-    n = moe_forward_launch_count(T)
+    n = moe_forward_launch_count_ex(T, schedule)
     us = (ctypes.c_float * max(n, 1))()
     _check(lib().moe_profile_forward(int(fmt), _p(x), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale),
                                      _p(out), T, H, I, int(E), int(k), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream),
                                      int(bool(prepacked_scales)), int(schedule), us),
            "moe_profile_forward")
-    names = KERNEL_NAMES if n == len(KERNEL_NAMES) else KERNEL_NAMES_SMALL
+    names = {len(KERNEL_NAMES): KERNEL_NAMES, len(KERNEL_NAMES_SMALL): KERNEL_NAMES_SMALL,
+             1: KERNEL_NAMES_FUSED}[n]
     return {names[i]: float(us[i]) for i in range(n)}
 
 

@@ -441,37 +441,9 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
 
   GemmParams p;
   memset(&p, 0, sizeof(p));
-  const int K = a.K;
-  const uint64_t act_row_bytes = ACT == 0 ? (uint64_t)K : (uint64_t)K / 2;
-  {
-    const cuuint64_t dims[2] = {act_row_bytes, (cuuint64_t)a.rows_cap};
-    const cuuint64_t strides[1] = {act_row_bytes};
-    const cuuint32_t box[2] = {128, (cuuint32_t)AROWS};
-    const cuuint32_t es[2] = {1, 1};
-    if (encode(&p.tmap_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.act), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t row_bytes = (uint64_t)K / 2;
-    const cuuint64_t strides[2] = {row_bytes, row_bytes * (uint64_t)a.N};
-    const cuuint32_t box[3] = {128, (cuuint32_t)kNTile, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    CUresult r;
-    if (ACT == 0) {  // packed FP4 in global, 8-byte gap after every 16 codes in shared memory
-      const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)a.N, (cuuint64_t)a.E};
-      r = encode(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(a.w), dims, strides, box,
-                 es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {  // packed FP4 kept packed
-      const cuuint64_t dims[3] = {row_bytes, (cuuint64_t)a.N, (cuuint64_t)a.E};
-      r = encode(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.w), dims, strides, box, es,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  }
+  if (!encode_act_map(&p.tmap_act, a.act, a.rows_cap, a.K, ACT, AROWS) ||
+      !encode_weight_map(&p.tmap_w, a.w, a.E, a.N, a.K, ACT))
+    return cudaErrorInvalidValue;
   if (EPI == 1) {
     const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.rows_cap};
     const cuuint64_t strides[1] = {(cuuint64_t)a.N * 2};

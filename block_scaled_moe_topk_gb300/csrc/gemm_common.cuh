@@ -211,5 +211,44 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// Tensor map of the activation codes [rows_cap, K] (E4M3: one byte per element; E2M1: two
+// per byte): box of 128 bytes x `arows` rows, 128-byte swizzle (the layout the MMA's shared
+// memory descriptors expect).  False if the driver rejects it.
+inline bool encode_act_map(CUtensorMap* m, const uint8_t* act, int64_t rows_cap, int K, int act_fmt, int arows) {
+  EncodeTiledFn encode = get_encode_fn();
+  if (!encode) return false;
+  const uint64_t row_bytes = act_fmt == 0 ? (uint64_t)K : (uint64_t)K / 2;
+  const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)rows_cap};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, (cuuint32_t)arows};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(act), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of the MXFP4 weights [E, N, K/2], box 128 K-elements x 256 rows x 1 expert.  With
+// E4M3 activations (kind::mxf8f6f4) the packed codes land with an 8-byte gap after every 8
+// bytes (16U4_ALIGN16B); with E2M1 activations (kind::mxf4) they stay packed.  Rows past N
+// (a 128-row last tile) read as zeros.
+inline bool encode_weight_map(CUtensorMap* m, const uint8_t* w, int E, int N, int K, int act_fmt) {
+  EncodeTiledFn encode = get_encode_fn();
+  if (!encode) return false;
+  const uint64_t row_bytes = (uint64_t)K / 2;
+  const cuuint64_t strides[2] = {row_bytes, row_bytes * (uint64_t)N};
+  const cuuint32_t box[3] = {128, (cuuint32_t)kNTile, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  if (act_fmt == 0) {
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)E};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(w), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[3] = {row_bytes, (cuuint64_t)N, (cuuint64_t)E};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(w), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace moe

@@ -78,7 +78,8 @@ moe_status_t layout(int64_t T, int H, int I, int E, int k, moe_act_fmt_t fmt, mo
     off = align256(off + bytes);
     return o;
   };
-  L->status = take(sizeof(uint32_t));
+  L->status = take(sizeof(uint32_t) * 8);
+  L->sync = take(sizeof(uint32_t) * moe::kSyncWords);  // right after the status words: one memset clears both
   L->topk_ids = take(sizeof(int32_t) * R);
   L->topk_w = take(sizeof(float) * R);
   L->counts = take(sizeof(int32_t) * E);
@@ -94,6 +95,10 @@ moe_status_t layout(int64_t T, int H, int I, int E, int k, moe_act_fmt_t fmt, mo
   L->a2 = take(ib * rows_cap);
   L->a2s = take((size_t)I / 32 * rows_cap);
   L->y2 = take(sizeof(uint16_t) * (size_t)H * rows_cap);
+  // the single-kernel decode schedule (T <= 64): partial accumulators and fp32 GEMM2 rows
+  const bool decode = T <= moe::kDecodeMaxTokens;
+  L->part = take(decode ? moe::decode_part_bytes(T) : 0);
+  L->y2f = take(decode ? sizeof(float) * (size_t)R * H : 0);
   L->total = off;
   L->rows_cap = rows_cap;
   L->nchunk = nchunk;
@@ -132,10 +137,17 @@ int test_stall_producer() {
 
 // The forward's launch sequence.  With `ev` (kForwardKernels + 1 events) an event is
 // recorded before the first kernel and after every kernel, for per-kernel timing.
-// T > 64: route, scan, scatter, quant, gemm1, gemm2, combine; T <= 64: route_sort, quant,
-// gemm1, gemm2, combine.
+// Kernel chain, T > 64: route, scan, scatter, quant, gemm1, gemm2, combine; T <= 64:
+// route_sort, quant, gemm1, gemm2, combine.  Fused schedule (T <= 64): one decode kernel.
 constexpr int kForwardKernels = 7;
-int launch_count(int64_t T) { return T <= 0 ? 0 : (T <= moe::kSmallRouteTokens ? 5 : kForwardKernels); }
+bool use_fused(int64_t T, int schedule) {
+  return schedule == MOE_SCHEDULE_FUSED || (schedule == MOE_SCHEDULE_AUTO && T <= moe::kDecodeAutoMaxTokens);
+}
+int launch_count(int64_t T, int schedule = MOE_SCHEDULE_AUTO) {
+  if (T <= 0) return 0;
+  if (use_fused(T, schedule)) return 1;
+  return T <= moe::kSmallRouteTokens ? 5 : kForwardKernels;
+}
 
 // x is bf16 [T, H] when x_scale is null, else prequantised codes [T, H or H/2] with canonical
 // E8M0 scales x_scale [T, H/32] (the quantiser is then replaced by a permuting copy).
@@ -152,7 +164,9 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
       !aligned(w1s, tiled_scales ? 16 : 4) || !aligned(w2s, tiled_scales ? 16 : 4) || !aligned(ws, 256))
     return MOE_ERR_MISALIGNED;
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN) return MOE_ERR_INVALID_ARG;
+  if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN && schedule != MOE_SCHEDULE_FUSED)
+    return MOE_ERR_INVALID_ARG;
+  if (schedule == MOE_SCHEDULE_FUSED && T > moe::kDecodeMaxTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
   DeviceInfo dev;
   st = device_info(&dev);
@@ -173,6 +187,53 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
 
   int evi = 0;
   auto mark = [&]() { return ev ? cudaEventRecord(ev[evi++], s) : cudaSuccess; };
+  const int afmt = fmt == MOE_ACT_MXFP8 ? 0 : 1;
+  if (use_fused(T, schedule) && dev.num_sms >= moe::kDecodeMaxTokens) {
+    // the status words and the decode kernel's counters start at zero on every call
+    MOE_CUDA_TRY(cudaMemsetAsync(W + L.status, 0, L.sync + sizeof(uint32_t) * moe::kSyncWords - L.status, s));
+    MOE_CUDA_TRY(mark());
+    moe::DecodeArgs da{};
+    da.act_fmt = afmt;
+    da.x = x_scale == nullptr ? static_cast<const uint16_t*>(x) : nullptr;
+    da.xq_in = x_scale == nullptr ? nullptr : static_cast<const uint8_t*>(x);
+    da.xs_in = x_scale;
+    da.logits = logits;
+    da.w1 = w1;
+    da.w1_sf = w1s;
+    da.w2 = w2;
+    da.w2_sf = w2s;
+    da.w_sf_tiled = tiled_scales ? 1 : 0;
+    da.rows_cap = L.rows_cap;
+    da.xq = at(L.xq);
+    da.xs = at(L.xs);
+    da.a2 = at(L.a2);
+    da.a2s = at(L.a2s);
+    da.part = reinterpret_cast<float*>(at(L.part));
+    da.y2f = reinterpret_cast<float*>(at(L.y2f));
+    da.out = static_cast<uint16_t*>(out);
+    da.ids = ids;
+    da.tw = tw;
+    da.counts = counts;
+    da.offsets = offsets;
+    da.padded_offsets = poff;
+    da.mtile_base = mtb;
+    da.sorted_pair = reinterpret_cast<int32_t*>(at(L.sorted_pair));
+    da.inv = reinterpret_cast<int32_t*>(at(L.inv));
+    da.inv_padded = inv_padded;
+    da.sync = reinterpret_cast<uint32_t*>(at(L.sync));
+    da.status = status;
+    da.timeout_ns = wait_timeout_ns();
+    da.num_sms = dev.num_sms;
+    da.test_stall = test_stall_producer();
+    da.T = T;
+    da.H = H;
+    da.I = I;
+    da.E = E;
+    da.k = k;
+    MOE_CUDA_TRY(moe::launch_decode(da, s));
+    MOE_CUDA_TRY(mark());
+    return MOE_OK;
+  }
   MOE_CUDA_TRY(mark());
   moe::RouteArgs ra{logits, T, E, k, ids, tw, chunk_hist, L.nchunk, status, 1};
   moe::SortArgs sa{ids, T, E, k, chunk_hist, L.nchunk, counts, offsets, poff, mtb,
@@ -189,7 +250,6 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
     MOE_CUDA_TRY(moe::launch_scatter(sa, s));
     MOE_CUDA_TRY(mark());
   }
-  const int afmt = fmt == MOE_ACT_MXFP8 ? 0 : 1;
   if (x_scale == nullptr) {
     moe::QuantArgs qa{static_cast<const uint16_t*>(x), T, H, afmt, at(L.xq), at(L.xs), inv_padded, k};
     MOE_CUDA_TRY(moe::launch_quant(qa, s));
@@ -420,6 +480,11 @@ moe_status_t moe_read_device_status(const void* ws, void* stream, moe_status_t* 
 
 int moe_forward_launch_count(int64_t T) { return launch_count(T); }
 
+int moe_forward_launch_count_ex(int64_t T, int schedule) {
+  if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN && schedule != MOE_SCHEDULE_FUSED) return -1;
+  return launch_count(T, schedule);
+}
+
 moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* logits, const uint8_t* w1,
                                  const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T,
                                  int H, int I, int E, int k, void* ws, size_t ws_bytes, void* stream,
@@ -433,7 +498,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* 
   if (st == MOE_OK)
     st = forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt,
                  prepacked_scales != 0, ev, schedule);
-  const int nk = launch_count(T);
+  const int nk = launch_count(T, schedule);
   if (st == MOE_OK && T > 0) {
     if (cudaEventSynchronize(ev[nk]) != cudaSuccess) st = MOE_ERR_CUDA;
     for (int i = 0; i < nk && st == MOE_OK; ++i) {

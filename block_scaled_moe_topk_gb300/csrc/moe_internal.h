@@ -126,6 +126,68 @@ constexpr int kUnit64MinStages = 16;
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 
 
+// decode.cu: the whole layer for a small batch in one persistent kernel (T <= kDecodeMaxTokens).
+// Every CTA routes and sorts the batch itself; CTA b quantises token b; GEMM1 and GEMM2 are
+// each spread over all CTAs by K stages; GEMM2 stages of an expert wait for its A2 rows; the
+// combine runs as each output column block completes.  Counters live in the workspace's
+// sync region, which the host zeroes before the launch.
+constexpr int kDecodeMaxTokens = kSmallRouteTokens;
+// MOE_SCHEDULE_AUTO takes the fused kernel up to this many tokens (measured on the GB300: it is
+// as fast or faster than the kernel chain there on every shape of the configs)
+constexpr int kDecodeAutoMaxTokens = 16;
+constexpr int kDecodeMaxPairs = kDecodeMaxTokens * kMaxTopK;  // routed rows, also active experts
+constexpr int kDecodeMaxCtas = 160;                           // grid = min(SMs, this)
+// sync region (uint32 words)
+constexpr int kSyncQuant = 0;                                     // tokens quantised
+constexpr int kSyncDone2 = 1;                                     // GEMM2 parts final
+constexpr int kSyncReady = 16;                                    // [active expert] GEMM1 parts final
+constexpr int kSyncTicket = kSyncReady + kDecodeMaxPairs;         // [phase][first CTA][warp] tickets
+constexpr int kSyncWords = kSyncTicket + 2 * kDecodeMaxCtas * 8;
+// activation rows staged per K stage: every expert of a batch of T tokens has at most T rows
+inline int decode_arows(int64_t T) { return T <= 16 ? 16 : 64; }
+// partial-accumulator slots: per CTA, per GEMM, its first and last item
+inline size_t decode_part_bytes(int64_t T) {
+  return (size_t)kDecodeMaxCtas * 4 * (size_t)decode_arows(T) * kNTile * sizeof(float);
+}
+
+struct DecodeArgs {
+  int act_fmt;
+  const uint16_t* x;          // bf16 [T, H], or null when the input is prequantised:
+  const uint8_t* xq_in;       //   codes [T, H or H/2]
+  const uint8_t* xs_in;       //   canonical E8M0 scales [T, H/32]
+  const float* logits;        // [T, E]
+  const uint8_t* w1;
+  const uint8_t* w1_sf;
+  const uint8_t* w2;
+  const uint8_t* w2_sf;
+  int w_sf_tiled;
+  int64_t rows_cap;
+  uint8_t* xq;                // padded expert rows + 128x4 tile scales (as the kernel chain)
+  uint8_t* xs;
+  uint8_t* a2;
+  uint8_t* a2s;
+  float* part;                // decode_part_bytes(T)
+  float* y2f;                 // fp32 GEMM2 rows [T*k, H], unpadded row order
+  uint16_t* out;              // bf16 [T, H]
+  int32_t* ids;               // routing / sort results, as the kernel chain writes them
+  float* tw;
+  int32_t* counts;
+  int64_t* offsets;
+  int64_t* padded_offsets;
+  int32_t* mtile_base;
+  int32_t* sorted_pair;
+  int32_t* inv;
+  int32_t* inv_padded;
+  uint32_t* sync;             // kSyncWords, zero at launch
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int num_sms;
+  int test_stall;
+  int64_t T;
+  int H, I, E, k;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
 // combine.cu
 struct CombineArgs {
   const uint16_t* y2;       // bf16 [rows_cap, H]

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   for (int64_t t = t_begin + warp; t < t_end; t += kRouteWarps) {
     int my_id;
     float my_w;
-    route_token<kPerLane>(a.logits + t * E, E, k, lane, my_id, my_w);
+    route_token_fast<kPerLane>(a.logits + t * E, E, k, lane, my_id, my_w);
     if (lane < k) {
       a.ids[t * k + lane] = my_id;
       a.w[t * k + lane] = my_w;

@@ -91,6 +91,88 @@ __device__ __forceinline__ void route_token(const float* l, int E, int k, int la
   w_out = __fdiv_rn(p, zh) * (1.0f - __fdiv_rn(zl, zh));
 }
 
+// Order-preserving 32-bit key of a non-NaN float (larger value, larger key); -0 and +0 share
+// the key of +0, as they compare equal.
+__device__ __forceinline__ uint32_t route_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float route_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// The same ranking and weights as route_token with a shorter dependency chain: each lane keeps
+// its best remaining expert, each of the k rounds takes the warp's maximum key and, among the
+// lanes holding it, the lowest expert index with two redux.sync reductions, and only the
+// winning lane rescans its values.  A selected -0 logit reports +0 (the same weight).
+template <int kMaxPerLane = kMaxExperts / 32>
+__device__ __forceinline__ void route_token_fast(const float* l, int E, int k, int lane, int& id_out, float& w_out) {
+  static_assert(kMaxPerLane <= 32, "availability-mask width");
+  const int per_lane = (E + 31) / 32;
+  uint32_t key[kMaxPerLane];
+  uint32_t avail = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    const bool in = i < per_lane && e < E;
+    const float x = in ? l[e] : 0.0f;
+    key[i] = route_key(x != x ? -INFINITY : x);  // a NaN logit ranks as -inf
+    if (in) avail |= 1u << i;
+  }
+  // this lane's best remaining expert: largest key, lowest index among equal keys (the first i)
+  uint32_t best = 0;
+  int best_i = -1;
+  auto rescan = [&]() {
+    best = 0;
+    best_i = -1;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i)
+      if (((avail >> i) & 1u) && (best_i < 0 || key[i] > best)) {
+        best = key[i];
+        best_i = i;
+      }
+  };
+  rescan();
+  int my_id = 0;
+  float my_val = 0.0f, lmax = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    // every available key is > 0 (route_key(-inf) = 0x007fffff), so 0 stands for "none left"
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, best_i >= 0 ? best : 0u);
+    const uint32_t mine = (best_i >= 0 && best == mk) ? (uint32_t)(lane + 32 * best_i) : 0xffffffffu;
+    const uint32_t mi = __reduce_min_sync(0xffffffffu, mine);
+    const float mv = route_key_value(mk);
+    if (j == 0) lmax = mv;
+    if (lane == j) {
+      my_id = (int)mi;
+      my_val = mv;
+    }
+    if ((int)(mi & 31u) == lane) {
+      avail &= ~(1u << (mi >> 5));
+      rescan();
+    }
+  }
+  // p_j = exp(l_j - l_max) and the compensated sum, exactly as route_token
+  float p = 0.0f;
+  if (lane < k) {
+    const float sdiff = my_val - lmax;
+    const float bb = sdiff - my_val;
+    const float e = (my_val - (sdiff - bb)) + (-lmax - bb);
+    p = sdiff == -INFINITY ? 0.0f : expf(sdiff) * (1.0f + e);
+  }
+  float zh = p, zl = 0.0f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, zh, off);
+    const float ol = __shfl_xor_sync(0xffffffffu, zl, off);
+    const float sum = zh + oh;
+    const float bv = sum - zh;
+    zl += ol + ((zh - (sum - bv)) + (oh - bv));
+    zh = sum;
+  }
+  id_out = my_id;
+  w_out = __fdiv_rn(p, zh) * (1.0f - __fdiv_rn(zl, zh));
+}
+
 // Eight lanes per token (lane g = lane % 8 of its group holds experts g + 8 i, i < kV), so a
 // warp routes four tokens at once with three butterfly levels per selection instead of five.
 // Same ranking and weights as route_token; kV >= ceil(E / 8), kV <= 64.  The local scan runs

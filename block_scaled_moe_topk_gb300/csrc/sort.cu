@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArg
   for (int64_t t = warp; t < T; t += kScanThreads / 32) {
     int id;
     float w;
-    route_token<kPerLane>(ra.logits + t * E, E, k, lane, id, w);
+    route_token_fast<kPerLane>(ra.logits + t * E, E, k, lane, id, w);
     if (lane < k) {
       ra.ids[t * k + lane] = id;
       ra.w[t * k + lane] = w;

@@ -87,15 +87,26 @@ typedef enum {
 /*
  * How a forward call schedules its work (moe_forward_ex, moe_profile_forward).
  *   MOE_SCHEDULE_CHAIN  the kernel chain: routing + sort, quantiser, GEMM1, GEMM2, combine;
- *                       each GEMM runs one CTA per 128-row x 256-column tile over the whole K.
- *   MOE_SCHEDULE_AUTO   the library's choice for the shape and T (every named entry point
- *                       uses this rule).
+ *                       each GEMM runs one CTA per 128-row x 256-column tile over the whole K;
+ *                       GEMM2 rows are stored as bf16 before the combine.
+ *   MOE_SCHEDULE_FUSED  T <= 64 only (else MOE_ERR_UNSUPPORTED_SHAPE): the whole layer in one
+ *                       persistent kernel on every SM ("feat(moe): FlyDSL MegaMoE fused EP-MoE
+ *                       integration", description: one fused step for dispatch + gemm1 + quant
+ *                       + gemm2 + combine).  Each CTA routes and sorts the batch itself; the
+ *                       K stages of each GEMM are split evenly over the CTAs, partial
+ *                       accumulators of an item cut between CTAs are summed in CTA order by
+ *                       the last contributor (deterministic); GEMM2 rows stay fp32 up to the
+ *                       combine.  Preceded by a memset of the workspace's status and sync words.
+ *   MOE_SCHEDULE_AUTO   the library's choice: FUSED for T <= 16, CHAIN above (every named
+ *                       entry point uses this rule).
  * Every schedule computes the same routing, permutation and quantised activations bit for
- * bit; outputs agree within the parity tolerance of the layer.
+ * bit; outputs agree within the parity tolerance of the layer, and each schedule is
+ * deterministic (repeated calls give the same bits).
  */
 typedef enum {
   MOE_SCHEDULE_AUTO = 0,
-  MOE_SCHEDULE_CHAIN = 1
+  MOE_SCHEDULE_CHAIN = 1,
+  MOE_SCHEDULE_FUSED = 2
 } moe_schedule_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -122,15 +133,21 @@ const char* moe_status_string(moe_status_t status);
  *   y2           bf16 [rows_cap, H]        GEMM2 output rows (unweighted; fp32-accumulated,
  *                                          rounded to bf16 like the pages' reduced-precision
  *                                          stage-2 transport)
+ *   part         fp32 partial accumulators of the fused schedule (T <= 64 only, else empty)
+ *   y2f          fp32 [T*k, H] GEMM2 rows of the fused schedule, unpadded row order
+ *                (T <= 64 only, else empty)
+ *   sync         uint32 counters of the fused schedule, zeroed by the forward before its launch
  *   status       uint32[8]: [0] device status bits (read them with moe_read_device_status);
  *                [1..6] the first expired in-kernel wait, if any: [1] = 1 when recorded,
- *                [2] barrier index, [3] phase parity, [4] CTA, [5] warp, [6] microseconds waited
+ *                [2] barrier index (1000 + word offset in `sync` for a counter of the fused
+ *                schedule), [3] phase parity (counter target), [4] CTA, [5] warp,
+ *                [6] microseconds waited
  * The 128x4 tile layout stores the scale of (row r, 32-block kb) at byte
  *   ((r/128)*(K/128) + kb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + kb%4.
  */
 typedef struct {
-  size_t status, topk_ids, topk_w, counts, offsets, padded_offsets, mtile_base, chunk_hist;
-  size_t sorted_pair, inv, inv_padded, xq, xs, a2, a2s, y2;
+  size_t status, sync, topk_ids, topk_w, counts, offsets, padded_offsets, mtile_base, chunk_hist;
+  size_t sorted_pair, inv, inv_padded, xq, xs, a2, a2s, y2, part, y2f;
   size_t total;      /* bytes needed == moe_workspace_bytes(...) */
   int64_t rows_cap;  /* padded row capacity (multiple of 128) */
   int64_t nchunk;    /* number of routing chunks (sort scratch width) */
@@ -322,9 +339,14 @@ moe_status_t moe_forward_ex(const moe_forward_args_t* args);
  */
 moe_status_t moe_read_device_status(const void* workspace, void* stream, moe_status_t* status_out);
 
-/* Number of kernels one forward call launches for T tokens: 0 for T = 0, 5 for
- * T <= 64 (routing and sort fused into one kernel), 7 above. */
+/* Number of kernels one forward call launches for T tokens under MOE_SCHEDULE_AUTO: 0 for
+ * T = 0, 1 for T <= 16 (the fused decode kernel), 5 for T <= 64, 7 above. */
 int moe_forward_launch_count(int64_t T);
+
+/* The same for a given schedule (moe_schedule_t): the kernel chain launches 5 kernels for
+ * T <= 64 (routing and sort in one kernel) and 7 above; the fused schedule 1.  Returns -1 for
+ * an unknown schedule. */
+int moe_forward_launch_count_ex(int64_t T, int schedule);
 
 /*
  * Profiling form of the forward: enqueues exactly the launch sequence of
@@ -333,9 +355,9 @@ int moe_forward_launch_count(int64_t T);
  * schedule `schedule` (moe_schedule_t, as in moe_forward_ex),
  * with a CUDA event recorded before the first kernel and after each kernel,
  * waits for the last event, and writes the duration of each kernel in
- * microseconds to kernel_us[moe_forward_launch_count(T)] (HOST array), in
- * launch order: route, scan, scatter, quant, gemm1, gemm2, combine (T > 64) or
- * route_sort, quant, gemm1, gemm2, combine (T <= 64).
+ * microseconds to kernel_us[moe_forward_launch_count_ex(T, schedule)] (HOST array),
+ * in launch order: route, scan, scatter, quant, gemm1, gemm2, combine (chain, T > 64),
+ * route_sort, quant, gemm1, gemm2, combine (chain, T <= 64) or decode (fused).
  * Arguments and errors as for the forward; additionally synchronises on its
  * own events (so it is not graph-capturable) and creates/destroys them.
  */

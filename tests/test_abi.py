@@ -45,10 +45,15 @@ def test_workspace_layout_and_bytes():
     L = moe.moe_get_workspace_layout(8192, 7168, 3072, 384, 6)
     R = 8192 * 6
     assert L.rows_cap % 128 == 0 and L.rows_cap >= R and L.rows_cap <= R + 127 * 384 + 127
-    offs = [L.status, L.topk_ids, L.topk_w, L.counts, L.offsets, L.padded_offsets, L.mtile_base, L.chunk_hist,
-            L.sorted_pair, L.inv, L.inv_padded, L.xq, L.xs, L.a2, L.a2s, L.y2]
+    offs = [L.status, L.sync, L.topk_ids, L.topk_w, L.counts, L.offsets, L.padded_offsets, L.mtile_base,
+            L.chunk_hist, L.sorted_pair, L.inv, L.inv_padded, L.xq, L.xs, L.a2, L.a2s, L.y2, L.part, L.y2f]
     assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
     assert L.y2 + 2 * 7168 * L.rows_cap <= L.total  # bf16 GEMM2 rows
+    assert L.part == L.y2f == L.total  # the fused schedule's buffers exist only for T <= 64
+    assert L.sync == 256  # right after the status words (one memset clears both)
+    small = moe.moe_get_workspace_layout(64, 7168, 3072, 384, 6)
+    assert small.y2f - small.part >= 160 * 4 * 64 * 256 * 4  # partial slots: CTAs x 4 x 64 rows x 256
+    assert small.total - small.y2f >= 64 * 6 * 7168 * 4      # fp32 GEMM2 rows
     assert moe.moe_workspace_bytes(8192, 7168, 3072, 384, 6) == L.total
     a4 = moe.moe_get_workspace_layout(8192, 7168, 3072, 384, 6, moe.MOE_ACT_MXFP4)
     assert a4.total < L.total
@@ -99,9 +104,14 @@ def test_forward_validation_before_any_launch():
 
 def test_forward_launch_count():
     assert moe.moe_forward_launch_count(0) == 0
-    assert moe.moe_forward_launch_count(1) == 5
-    assert moe.moe_forward_launch_count(64) == 5
+    assert moe.moe_forward_launch_count(1) == 1      # fused decode kernel
+    assert moe.moe_forward_launch_count(16) == 1
+    assert moe.moe_forward_launch_count(17) == 5     # kernel chain, routing + sort in one kernel
     assert moe.moe_forward_launch_count(65) == 7
+    assert moe.moe_forward_launch_count_ex(64, moe.MOE_SCHEDULE_CHAIN) == 5
+    assert moe.moe_forward_launch_count_ex(65, moe.MOE_SCHEDULE_CHAIN) == 7
+    assert moe.moe_forward_launch_count_ex(3, moe.MOE_SCHEDULE_FUSED) == 1
+    assert moe.moe_forward_launch_count_ex(3, 9) == -1
 
 
 def test_forward_ex_schedule_validation():
@@ -113,3 +123,7 @@ def test_forward_ex_schedule_validation():
     assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 1
     a.schedule = -1
     assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 1
+    a.schedule = moe.MOE_SCHEDULE_FUSED
+    a.T = 65  # the fused schedule takes at most 64 tokens
+    a.workspace_bytes = moe.moe_workspace_bytes(65, 256, 128, 8, 2)
+    assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 2

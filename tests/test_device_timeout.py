@@ -30,7 +30,7 @@ x, lg = synth.x_bf16(T, s.H, 0, device=dev), synth.gate_logits(T, s.E, 0, device
 out = torch.zeros(T, s.H, dtype=torch.bfloat16, device=dev)
 ws = torch.zeros(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=dev)
 t0 = time.time()
-moe.moe_a8w4_forward(x, lg, *W, out, s.E, s.k, ws)
+moe.moe_forward_ex(x, lg, *W, out, s.E, s.k, ws, schedule=int(sys.argv[2]))
 torch.cuda.synchronize()
 dt = time.time() - t0
 status = moe.moe_read_device_status(ws)
@@ -40,11 +40,13 @@ print(json.dumps({"status": status, "words": words, "alive": alive, "seconds": d
 """
 
 
-def test_expired_wait_is_reported_and_the_context_survives():
+@pytest.mark.parametrize("schedule", ["chain", "fused"])
+def test_expired_wait_is_reported_and_the_context_survives(schedule):
     import __graft_entry__
     __graft_entry__.build()
     env = dict(os.environ, MOE_TEST_STALL_PRODUCER="1", MOE_WAIT_TIMEOUT_NS="50000000")  # 50 ms
-    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True, text=True,
+    sched = {"chain": 1, "fused": 2}[schedule]
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(sched)], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     d = json.loads(r.stdout.strip().splitlines()[-1])
@@ -52,10 +54,15 @@ def test_expired_wait_is_reported_and_the_context_survives():
     words = d["words"]
     assert words[1] == 1                 # an expiry was recorded
     # the first expiry: stage 0's full barrier in the MMA warp (index 0, warp 1) or the
-    # accumulator-ready barrier in an epilogue warp (index 2 * stages: 12 with the 6-stage
-    # ring of 16-row slots), warps 2-9, whichever came first
+    # accumulator-ready barrier in an epilogue warp (index 2 * stages = 12: both schedules run a
+    # 6-stage ring for 16-row slots), warps 2-9, or -- fused schedule -- the combine's wait for
+    # every GEMM2 part in a CTA with no work of its own (1000 + its sync word offset 1),
+    # whichever came first
     acc_ready = 12
-    assert (words[2], words[5]) == (0, 1) or (words[2] == acc_ready and 2 <= words[5] <= 9), words
+    ok = (words[2], words[5]) == (0, 1) or (words[2] == acc_ready and 2 <= words[5] <= 9)
+    if schedule == "fused":
+        ok = ok or (words[2] == 1001 and 2 <= words[5] <= 9)
+    assert ok, words
     assert words[6] >= 25000             # it waited the limit (>= 50 ms at <= 2 GHz), in us
     assert d["alive"] == 999000.0        # the context still runs kernels
     assert d["seconds"] < 60

@@ -387,8 +387,9 @@ def test_profile_forward_matches_forward():
     out_a = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
     out_b = torch.empty_like(out_a)
     ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
-    moe.moe_a8w4_forward(x, lg, *W.dev, out_a, s.E, s.k, ws)
-    us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws)
+    moe.moe_forward_ex(x, lg, *W.dev, out_a, s.E, s.k, ws, schedule=moe.MOE_SCHEDULE_CHAIN)
+    us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws,
+                                 schedule=moe.MOE_SCHEDULE_CHAIN)
     torch.cuda.synchronize()
     assert list(us) == list(moe.KERNEL_NAMES_SMALL) and all(v > 0 for v in us.values())
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
@@ -539,3 +540,113 @@ def test_forward_hidden_size_not_a_multiple_of_256(act, H, I, T):
 def test_forward_tp_shard_shapes(shape, T):
     """The remaining per-rank shapes of the tuned grid (inter 1152 at 384x6, inter 640 at 128x3)."""
     _sampled_check(moe.MOE_ACT_MXFP8, synth.SHAPES[shape], T, 32)
+
+
+# --------------------------------------------------------------------------- fused decode schedule
+DECODE_CASES = [("flash_decode", 1), ("flash_decode", 2), ("flash_decode", 4), ("flash_decode", 8),
+                ("flash_decode", 16), ("flash_decode", 32), ("flash_decode", 64), ("draft", 1), ("draft", 16),
+                ("draft", 64), ("draft_tp4", 3), ("draft_tp4", 40), ("flash_tp2", 1), ("flash_tp2", 48)]
+
+
+@pytest.mark.parametrize("schedule", [moe.MOE_SCHEDULE_CHAIN, moe.MOE_SCHEDULE_FUSED])
+@pytest.mark.parametrize("shape,T", DECODE_CASES)
+def test_decode_schedules_against_oracle(schedule, shape, T):
+    """Both schedules of a decode-sized batch, every token against the oracle."""
+    _sampled_check(moe.MOE_ACT_MXFP8, synth.SHAPES[shape], T, T, seed=T, schedule=schedule)
+
+
+@pytest.mark.parametrize("shape,T", [("flash_decode", 8), ("draft", 33), ("tiny", 16)])
+def test_fused_a4w4_against_oracle(shape, T):
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 5), synth.gate_logits(T, s.E, 5, skew=s.skew)
+    out, ws = _run_forward(moe.MOE_ACT_MXFP4, x, lg, W, s.E, s.k, schedule=moe.MOE_SCHEDULE_FUSED)
+    _check_intermediates(moe.MOE_ACT_MXFP4, x, lg, W, s.E, s.k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, moe.MOE_ACT_MXFP4)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("T", [1, 16, 64])
+def test_fused_pro_against_oracle(act, T):
+    _sampled_check(act, synth.SHAPES["pro"], T, T, seed=1, schedule=moe.MOE_SCHEDULE_FUSED)
+
+
+def test_fused_1024_experts_top8_fills_the_tables():
+    """T * k = 512 routed rows (the fused schedule's table size) over 1024 experts, routed a warp
+    per token (E > 512)."""
+    E, k, H, I, T = 1024, 8, 256, 128, 64
+    W = Weights(E, H, I, seed=5, device=DEV)
+    x, lg = synth.x_bf16(T, H, 6), synth.gate_logits(T, E, 6)
+    out, ws = _run_forward(moe.MOE_ACT_MXFP8, x, lg, W, E, k, schedule=moe.MOE_SCHEDULE_FUSED)
+    _check_intermediates(moe.MOE_ACT_MXFP8, x, lg, W, E, k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, oracle.FMT_E4M3)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("shape,T", [("flash_decode", 1), ("flash_decode", 37), ("draft", 64)])
+def test_fused_is_deterministic_and_layout_independent(act, shape, T):
+    """The fused schedule gives the same bits on repeated calls, on a workspace full of stale
+    random bytes, with canonical or prepacked weight scales, and as CUDA-graph replays."""
+    s = synth.SHAPES[shape]
+    W = _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 7).to(DEV), synth.gate_logits(T, s.E, 7, skew=s.skew).to(DEV)
+    nbytes = moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act)
+    gen = torch.Generator(device=DEV).manual_seed(9)
+    outs = []
+    for fill, weights, prepacked in (("zeros", W.dev, False), ("zeros", W.dev, False),
+                                     ("random", W.dev, False), ("random", W.dev_prepacked(), True)):
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+        if fill == "random":
+            ws.random_(0, 256, generator=gen)
+        out = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+        moe.moe_forward_ex(x, lg, *weights, out, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=prepacked,
+                           schedule=moe.MOE_SCHEDULE_FUSED)
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(ws) == 0
+        outs.append(out)
+    out_g = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        moe.moe_forward_ex(x, lg, *W.dev_prepacked(), out_g, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=True,
+                           schedule=moe.MOE_SCHEDULE_FUSED, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    outs.append(out_g)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("entry", ["prequant", "ex"])
+def test_fused_prequant_against_oracle(entry):
+    s = synth.SHAPES["flash_decode"]
+    T = 24
+    W = _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 8), synth.gate_logits(T, s.E, 8)
+    out, ws = _run_forward(moe.MOE_ACT_MXFP8, x, lg, W, s.E, s.k, entry=entry, schedule=moe.MOE_SCHEDULE_FUSED)
+    _check_intermediates(moe.MOE_ACT_MXFP8, x, lg, W, s.E, s.k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, oracle.FMT_E4M3)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+def test_profile_forward_fused():
+    s = synth.SHAPES["flash_decode"]
+    W = _weights(s)
+    T = 4
+    x, lg = synth.x_bf16(T, s.H, 0).to(DEV), synth.gate_logits(T, s.E, 0).to(DEV)
+    out_a = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+    out_b = torch.empty_like(out_a)
+    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
+    moe.moe_a8w4_forward(x, lg, *W.dev, out_a, s.E, s.k, ws)
+    us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws)
+    torch.cuda.synchronize()
+    assert list(us) == ["decode"] and us["decode"] > 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
