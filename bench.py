@@ -479,7 +479,7 @@ def run_ours(args):
                        "hbm_frac": round(th / (ms_per_step / 1e3), 4),
                        "tensor_frac": round(tt / (ms_per_step / 1e3), 4), "peaks": pk["source"]},
         "roofline": roofline, "kernel_us": {n: round(v, 2) for n, v in kern_us.items()},
-        "e2e": e2e, "gpu_launches": args.steps * moe.moe_forward_launch_count(T),
+        "e2e": e2e, "gpu_launches": args.steps * moe.moe_forward_launch_count(T, H, I),
         "device_status": status, "sweep": rows, "clocks": clk, "cpu_baseline": cpu,
     }
     if world > 1:

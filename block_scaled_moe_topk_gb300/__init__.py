@@ -91,9 +91,9 @@ def lib():
     L.moe_read_device_status.restype = i32
     L.moe_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
     L.moe_forward_launch_count.restype = i32
-    L.moe_forward_launch_count.argtypes = [i64]
+    L.moe_forward_launch_count.argtypes = [i64, i32, i32]
     L.moe_forward_launch_count_ex.restype = i32
-    L.moe_forward_launch_count_ex.argtypes = [i64, i32]
+    L.moe_forward_launch_count_ex.argtypes = [i64, i32, i32, i32]
     L.moe_profile_forward.restype = i32
     L.moe_profile_forward.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P, i32, i32,
                                       ctypes.POINTER(ctypes.c_float)]
@@ -141,12 +141,12 @@ def moe_workspace_bytes(T, H, I, E, k, fmt=MOE_ACT_MXFP8) -> int:
     return int(lib().moe_workspace_bytes(int(T), int(H), int(I), int(E), int(k), int(fmt)))
 
 
-def moe_forward_launch_count(T) -> int:
-    return int(lib().moe_forward_launch_count(int(T)))
+def moe_forward_launch_count(T, H, I) -> int:
+    return int(lib().moe_forward_launch_count(int(T), int(H), int(I)))
 
 
-def moe_forward_launch_count_ex(T, schedule) -> int:
-    return int(lib().moe_forward_launch_count_ex(int(T), int(schedule)))
+def moe_forward_launch_count_ex(T, H, I, schedule) -> int:
+    return int(lib().moe_forward_launch_count_ex(int(T), int(H), int(I), int(schedule)))
 
 
 def moe_topk_route(gate_logits, k, topk_ids, topk_w, stream=None):
@@ -266,7 +266,7 @@ def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E,
     """One forward with a CUDA event between kernels; returns {kernel name: microseconds}."""
     T, H = x.shape
     I = w2.shape[-1] * 2
-    n = moe_forward_launch_count_ex(T, schedule)
+    n = moe_forward_launch_count_ex(T, H, I, schedule)
     us = (ctypes.c_float * max(n, 1))()
     _check(lib().moe_profile_forward(int(fmt), _p(x), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale),
                                      _p(out), T, H, I, int(E), int(k), _p(workspace),

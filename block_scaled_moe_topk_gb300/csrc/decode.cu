@@ -82,8 +82,16 @@ struct DGeo {
   static_assert(kBOff % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
   static_assert(kSmemBytes <= 232448, "decode kernel shared memory");
   static_assert(kStages * 32 <= 256, "TMEM scale slots");
-  // the prologue's scratch (histogram, fill counters, pair ids and padded rows) sits in the ring
-  static_assert(kStages * kStageBytes >= 4 * (2 * (kMaxExperts + 1) + 2 * kDecodeMaxPairs), "prologue scratch");
+  // the prologue's scratch sits in the last ring slot, at these byte offsets: the expert
+  // histogram (int [E+1]), the per-active-expert token masks (uint64), pair ids and padded rows
+  // (int), then the staged quantised row of at most kDecodeMaxHidden elements and its scales
+  static constexpr int kScrMaskOff = (4 * (kMaxExperts + 1) + 127) / 128 * 128;
+  static constexpr int kScrPairIdOff = kScrMaskOff + 8 * kDecodeMaxPairs;
+  static constexpr int kScrPairInvpOff = kScrPairIdOff + 4 * kDecodeMaxPairs;
+  static constexpr int kStageCodesOff = (kScrPairInvpOff + 4 * kDecodeMaxPairs + 127) / 128 * 128;
+  static_assert(kScrMaskOff % 8 == 0, "64-bit token masks");
+  static_assert(kStageBytes >= kStageCodesOff + kDecodeMaxHidden + kDecodeMaxHidden / 32, "prologue scratch");
+  static_assert(kStageCodesOff % 16 == 0, "16-byte accesses to the staged row");
 };
 
 struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
@@ -274,14 +282,16 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
   float* pair_w = reinterpret_cast<float*>(act_e + 4 * kDecodeMaxPairs);
   int16_t* pair_inv = reinterpret_cast<int16_t*>(pair_w + kDecodeMaxPairs);  // unpadded row of pair q
   Phase* phs = reinterpret_cast<Phase*>(pair_inv + kDecodeMaxPairs);
-  // prologue scratch in the last ring slot: the scatter (warp 0) and the quantiser (warps 2..9)
+  // prologue scratch in the last ring slot: the scatter (warps 0, 2..9) and the quantiser (warps 2..9)
   // still read it after the producers start; the weight producer enters that slot only after
   // the quantiser's warps release it, the activation producer only after the quant count
   // (which includes this CTA's own quantiser)
   int* hist = reinterpret_cast<int*>(smem + (kStages - 1) * kStageBytes);
-  int* fill = hist + kMaxExperts + 1;
-  int* pair_id = fill + kMaxExperts + 1;
-  int* pair_invp = pair_id + kDecodeMaxPairs;  // padded row of pair q
+  // per active expert, the set of tokens routed to it (T <= 64: one bit per token); a pair's
+  // rank inside its expert's group is the number of earlier tokens in that set
+  unsigned long long* tok_mask = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(hist) + G::kScrMaskOff);
+  int* pair_id = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(hist) + G::kScrPairIdOff);
+  int* pair_invp = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(hist) + G::kScrPairInvpOff);  // padded row of pair q
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int T = p.T, E = p.E, k = p.k, H = p.H, I = p.I;
@@ -301,6 +311,7 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     tmem_holder[3] = 0;  // set once the prologue's scratch (in the last ring slot) is free
+    tmem_holder[4] = 1;  // routing available (cleared if the published routing never completes)
     fence_mbar_init();
     prefetch_tensormap(&p.tmap_x);
     prefetch_tensormap(&p.tmap_w1);
@@ -318,33 +329,139 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
     const uintptr_t hi = (reinterpret_cast<uintptr_t>(p.logits + (int64_t)T * E)) & ~uintptr_t(15);
     if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
   }
-  for (int e = threadIdx.x; e < E; e += kDThreads) {
-    hist[e] = 0;
-    fill[e] = 0;
-  }
+  for (int e = threadIdx.x; e < E; e += kDThreads) hist[e] = 0;
+  for (int i = threadIdx.x; i < kDecodeMaxPairs; i += kDThreads) tok_mask[i] = 0;
   __syncthreads();
 
-  // ---------------------------------------------------------------- routing (every CTA)
-  // A warp per token (warp w: tokens w, w + 11, ...): no CTA waits for another before its
-  // weights start to stream, and a decode step's latency is one token's top-k.
-  for (int t = warp; t < T; t += kDWarps) {
+  // ---------------------------------------------------------------- quantise token b (b < T)
+  // into shared memory (warps 2..9), while the other warps route: only the copy to the k padded
+  // expert rows waits for the sort.  16 elements per thread, lanes 2m and 2m+1 share a block.
+  // (16-byte stores and loads: the staging area starts on a 128-byte boundary of the slot)
+  uint8_t* stage_codes = reinterpret_cast<uint8_t*>(hist) + G::kStageCodesOff;
+  uint8_t* stage_sf = stage_codes + (ACT == 0 ? H : H / 2);
+  const int row_bytes = ACT == 0 ? H : H / 2;
+  if (b < T && warp >= 2 && warp < 2 + kDEpiWarps) {
+    const int et = threadIdx.x - 64;
+    if (p.x != nullptr) {
+      const int chunks = H / 16;
+      for (int base = et - lane; base < chunks; base += 32 * kDEpiWarps) {  // warp-uniform
+        const int c = base + lane;
+        const bool active = c < chunks;
+        float v[16];
+        if (active) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.x + (int64_t)b * H + c * 16);
+          const uint4 r0 = src[0], r1 = src[1];
+          const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            v[2 * q] = __uint_as_float(w[q] << 16);
+            v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        if (!active) continue;
+        const MxScale sc = mx_scale<ACT>(amax);
+        if (ACT == 0) {
+          const uint2 c0 = pack_e4m3x8(v, sc.mult), c1 = pack_e4m3x8(v + 8, sc.mult);
+          *reinterpret_cast<uint4*>(stage_codes + c * 16) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+        } else {
+          *reinterpret_cast<uint2*>(stage_codes + c * 8) = make_uint2(pack_e2m1x8(v, sc.mult), pack_e2m1x8(v + 8, sc.mult));
+        }
+        if ((c & 1) == 0) stage_sf[c / 2] = sc.byte;
+      }
+    } else {
+      // prequantised input: token b's codes and canonical scales
+      for (int c = et; c < row_bytes / 16; c += 32 * kDEpiWarps)
+        *reinterpret_cast<uint4*>(stage_codes + c * 16) =
+            *reinterpret_cast<const uint4*>(p.xq_in + (int64_t)b * row_bytes + c * 16);
+      for (int kb = et; kb < H / 32; kb += 32 * kDEpiWarps) stage_sf[kb] = p.xs_in[(int64_t)b * (H / 32) + kb];
+    }
+  }
+
+  // ---------------------------------------------------------------- routing
+  // Up to 11 tokens every CTA routes the whole batch itself (a warp per token; warps 0, 1, 10
+  // first, the quantising warps after): no CTA waits for another before its weights start to
+  // stream.  Above that CTA b routes token b alone and publishes it (ids and weights in the
+  // workspace, a counter), and every CTA reads the batch back once all T are published.
+  const bool distributed = T > kDWarps;
+  auto route_one = [&](int t, bool publish) {
     int id;
     float w;
     const float* l = p.logits + (int64_t)t * E;
     if (E <= 512) route_token_fast<16>(l, E, k, lane, id, w);
     else route_token_fast<kMaxExperts / 32>(l, E, k, lane, id, w);
     if (lane < k) {
-      pair_id[t * k + lane] = id;
-      pair_w[t * k + lane] = w;
-      atomicAdd(&hist[id], 1);
-      if (b == 0) {
+      if (!distributed) {
+        pair_id[t * k + lane] = id;
+        pair_w[t * k + lane] = w;
+        atomicAdd(&hist[id], 1);
+      }
+      if (publish) {
         p.ids[t * k + lane] = id;
         p.tw[t * k + lane] = w;
       }
     }
+  };
+  if (!distributed) {
+    const int t = warp == 0 ? 0 : warp == 1 ? 1 : warp == kDWarps - 1 ? 2 : warp + 1;
+    if (t < T) route_one(t, b == 0);
+    __syncthreads();
+  } else {
+    if (warp == 0) {
+      if (b < T) {
+        route_one(b, true);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.sync + kSyncRouted, 1u);
+      }
+      if (lane == 0 && !wait_counter(p.sync + kSyncRouted, (uint32_t)T, p.sync, sync, p.timeout_ns))
+        tmem_holder[4] = 0;
+    }
+    __syncthreads();
+    if (tmem_holder[4] != 0) {
+      for (int q = threadIdx.x; q < R; q += kDThreads) {
+        const int id = __ldcg(p.ids + q);
+        pair_id[q] = id;
+        pair_w[q] = __ldcg(p.tw + q);
+        atomicAdd(&hist[id], 1);
+      }
+    }
+    // (a routing wait that expired leaves the histogram empty: no expert is active, nothing is
+    // scheduled, the scatter, copy and combine are skipped, and the status word carries the
+    // timeout)
+    __syncthreads();
   }
-  __syncthreads();
+  const bool routed = tmem_holder[4] != 0;
   const bool writer = b == 0;  // CTA 0 writes the sort to the workspace
+  // The stable scatter of the T*k pairs, on warp 0 and warps 2..9 (u = 0..287): token masks,
+  // then every pair's rank and rows; named barrier 3 between the passes.
+  auto scatter_pairs = [&](int u) {
+    constexpr int kU = 32 + 32 * kDEpiWarps;
+    if (routed)
+      for (int q = u; q < R; q += kU) atomicOr(&tok_mask[hist[pair_id[q]]], 1ull << (q / k));
+    named_barrier(3, kU);
+    if (routed)
+      for (int q = u; q < R; q += kU) {
+        const int t = q / k;
+        const int a = hist[pair_id[q]];
+        const int local = __popcll(tok_mask[a] & ((1ull << t) - 1ull));
+        const int r = act_off[a] + local;
+        const int rp = kRowTile * act_mtb[a] + local;
+        pair_inv[q] = (int16_t)r;
+        pair_invp[q] = rp;
+        if (writer) {
+          p.sorted_pair[r] = q;
+          p.inv[q] = r;
+          p.inv_padded[q] = rp;
+        }
+      }
+  };
   if (warp == 0) {
     // prefixes over experts (lane L owns experts [L * per, L * per + per)): unpadded rows,
     // 128-row tiles and the active-expert index; hist[e] becomes e's active index
@@ -433,38 +550,11 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
   }
 
   if (warp == 0) {
-    // ------------------------------------------------------------ pair scatter, then the
-    // activation producer.  Stable scatter of the pairs in ascending order (rank among equal
-    // experts by match); the quantiser (warps 2..9) waits for it at named barrier 1.
-    {
-      const uint32_t lt_mask = (1u << lane) - 1u;
-      for (int q0 = 0; q0 < R; q0 += 32) {
-        const int q = q0 + lane;
-        const bool valid = q < R;
-        const int id = valid ? pair_id[q] : -1 - lane;
-        const uint32_t peers = __match_any_sync(0xffffffffu, id);
-        const int rank = __popc(peers & lt_mask);
-        const int leader = __ffs(peers) - 1;
-        const int a = valid ? hist[id] : 0;
-        const int base = valid ? fill[a] : 0;
-        __syncwarp();
-        if (valid && lane == leader) fill[a] = base + __popc(peers);
-        __syncwarp();
-        if (valid) {
-          const int local = base + rank;
-          const int r = act_off[a] + local;
-          const int rp = kRowTile * act_mtb[a] + local;
-          pair_inv[q] = (int16_t)r;
-          pair_invp[q] = rp;
-          if (writer) {
-            p.sorted_pair[r] = q;
-            p.inv[q] = r;
-            p.inv_padded[q] = rp;
-          }
-        }
-      }
-      named_barrier(1, 32 + 32 * kDEpiWarps);
-    }
+    // ------------------------------------------------------------ pair scatter (with warps
+    // 2..9), then the activation producer.  Pairs in (expert, token) order: pair q = (t, j) of
+    // active expert a goes to row act_off[a] + (number of tokens below t routed to a).
+    scatter_pairs(lane);
+    named_barrier(1, 32 + 32 * kDEpiWarps);
     if (lane == 0) {
       int slot = 0;
       uint32_t phase = 0;
@@ -667,67 +757,24 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ warps 2..9
     const int et = threadIdx.x - 64;  // 0..255
+    scatter_pairs(32 + et);
     named_barrier(1, 32 + 32 * kDEpiWarps);  // the pair scatter is done
-    // quantise token b (b < T) into its k padded expert rows: 16 elements per thread, lanes
-    // 2m and 2m+1 share a 32-block
-    if (b < T) {
-      const int t = b;
-      const int chunks = H / 16;
-      if (p.x != nullptr) {
-        for (int base = et - lane; base < chunks; base += 32 * kDEpiWarps) {  // warp-uniform
-          const int c = base + lane;
-          const bool active = c < chunks;
-          float v[16];
-          if (active) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.x + (int64_t)t * H + c * 16);
-            const uint4 r0 = src[0], r1 = src[1];
-            const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              v[2 * q] = __uint_as_float(w[q] << 16);
-              v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) v[q] = 0.0f;
-          }
-          float amax = 0.0f;
-#pragma unroll
-          for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-          if (!active) continue;
-          const MxScale sc = mx_scale<ACT>(amax);
-          const int kb = c / 2;
-          for (int j = 0; j < k; ++j) {
-            const int64_t prow = pair_invp[t * k + j];
-            if (ACT == 0) {
-              const uint2 c0 = pack_e4m3x8(v, sc.mult), c1 = pack_e4m3x8(v + 8, sc.mult);
-              *reinterpret_cast<uint4*>(p.xq + prow * H + c * 16) = make_uint4(c0.x, c0.y, c1.x, c1.y);
-            } else {
-              *reinterpret_cast<uint2*>(p.xq + prow * (H / 2) + c * 8) =
-                  make_uint2(pack_e2m1x8(v, sc.mult), pack_e2m1x8(v + 8, sc.mult));
-            }
-            if ((c & 1) == 0) p.xs[sf_tile_offset(prow, kb, H)] = sc.byte;
-          }
-        }
-      } else {
-        // prequantised input: token t's code row and scales copied to its k padded rows
-        const int row_bytes = ACT == 0 ? H : H / 2;
-        for (int c = et; c < row_bytes / 16; c += 32 * kDEpiWarps) {
-          const uint4 v = *reinterpret_cast<const uint4*>(p.xq_in + (int64_t)t * row_bytes + c * 16);
-          for (int j = 0; j < k; ++j)
-            *reinterpret_cast<uint4*>(p.xq + (int64_t)pair_invp[t * k + j] * row_bytes + c * 16) = v;
-        }
-        for (int kb = et; kb < H / 32; kb += 32 * kDEpiWarps) {
-          const uint8_t v = p.xs_in[(int64_t)t * (H / 32) + kb];
-          for (int j = 0; j < k; ++j) p.xs[sf_tile_offset(pair_invp[t * k + j], kb, H)] = v;
-        }
+    // token b's quantised row (staged at the start) into its k padded expert rows
+    if (b < T && routed) {
+      for (int c = et; c < row_bytes / 16; c += 32 * kDEpiWarps) {
+        const uint4 v = *reinterpret_cast<const uint4*>(stage_codes + c * 16);
+        for (int j = 0; j < k; ++j)
+          *reinterpret_cast<uint4*>(p.xq + (int64_t)pair_invp[b * k + j] * row_bytes + c * 16) = v;
+      }
+      for (int kb = et; kb < H / 32; kb += 32 * kDEpiWarps) {
+        const uint8_t v = stage_sf[kb];
+        for (int j = 0; j < k; ++j) p.xs[sf_tile_offset(pair_invp[b * k + j], kb, H)] = v;
       }
       __threadfence();
     }
     named_barrier(2, 32 * kDEpiWarps);
     if (et == 0) {
-      if (b < T) {
+      if (b < T && routed) {
         fence_proxy_async_global();  // the codes are read by other CTAs' TMA loads
         atomicAdd(p.sync + kSyncQuant, 1u);
       }
@@ -875,7 +922,7 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
     // out[t, n] = bf16(sum_j w[t, j] * y2[row(t, j), n]) in slot order with fp32 accumulation,
     // once every GEMM2 part is final; warp w of CTA b takes (token, 128-column block) units
     // b * 8 + w, + 8 * gridDim.x, ...; lane l owns 4 columns.
-    if (ok) {
+    if (ok && routed) {
       uint32_t parts = 0;
       for (int i = lane; i < n_act; i += 32) parts += (uint32_t)quads_of(i);
 #pragma unroll

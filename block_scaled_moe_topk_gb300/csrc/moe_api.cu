@@ -140,12 +140,12 @@ int test_stall_producer() {
 // Kernel chain, T > 64: route, scan, scatter, quant, gemm1, gemm2, combine; T <= 64:
 // route_sort, quant, gemm1, gemm2, combine.  Fused schedule (T <= 64): one decode kernel.
 constexpr int kForwardKernels = 7;
-bool use_fused(int64_t T, int schedule) {
-  return schedule == MOE_SCHEDULE_FUSED || (schedule == MOE_SCHEDULE_AUTO && T <= moe::kDecodeAutoMaxTokens);
+bool use_fused(int64_t T, int schedule, int H, int I) {
+  return schedule == MOE_SCHEDULE_FUSED || (schedule == MOE_SCHEDULE_AUTO && moe::decode_auto(T, H, I));
 }
-int launch_count(int64_t T, int schedule = MOE_SCHEDULE_AUTO) {
+int launch_count(int64_t T, int H, int I, int schedule = MOE_SCHEDULE_AUTO) {
   if (T <= 0) return 0;
-  if (use_fused(T, schedule)) return 1;
+  if (use_fused(T, schedule, H, I)) return 1;
   return T <= moe::kSmallRouteTokens ? 5 : kForwardKernels;
 }
 
@@ -166,7 +166,8 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN && schedule != MOE_SCHEDULE_FUSED)
     return MOE_ERR_INVALID_ARG;
-  if (schedule == MOE_SCHEDULE_FUSED && T > moe::kDecodeMaxTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (schedule == MOE_SCHEDULE_FUSED && (T > moe::kDecodeMaxTokens || H > moe::kDecodeMaxHidden))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
   DeviceInfo dev;
   st = device_info(&dev);
@@ -188,7 +189,7 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   int evi = 0;
   auto mark = [&]() { return ev ? cudaEventRecord(ev[evi++], s) : cudaSuccess; };
   const int afmt = fmt == MOE_ACT_MXFP8 ? 0 : 1;
-  if (use_fused(T, schedule) && dev.num_sms >= moe::kDecodeMaxTokens) {
+  if (use_fused(T, schedule, H, I) && dev.num_sms >= moe::kDecodeMaxTokens) {
     // the status words and the decode kernel's counters start at zero on every call
     MOE_CUDA_TRY(cudaMemsetAsync(W + L.status, 0, L.sync + sizeof(uint32_t) * moe::kSyncWords - L.status, s));
     MOE_CUDA_TRY(mark());
@@ -478,11 +479,11 @@ moe_status_t moe_read_device_status(const void* ws, void* stream, moe_status_t* 
   return MOE_OK;
 }
 
-int moe_forward_launch_count(int64_t T) { return launch_count(T); }
+int moe_forward_launch_count(int64_t T, int H, int I) { return launch_count(T, H, I); }
 
-int moe_forward_launch_count_ex(int64_t T, int schedule) {
+int moe_forward_launch_count_ex(int64_t T, int H, int I, int schedule) {
   if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN && schedule != MOE_SCHEDULE_FUSED) return -1;
-  return launch_count(T, schedule);
+  return launch_count(T, H, I, schedule);
 }
 
 moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* logits, const uint8_t* w1,
@@ -498,7 +499,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* 
   if (st == MOE_OK)
     st = forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt,
                  prepacked_scales != 0, ev, schedule);
-  const int nk = launch_count(T, schedule);
+  const int nk = launch_count(T, H, I, schedule);
   if (st == MOE_OK && T > 0) {
     if (cudaEventSynchronize(ev[nk]) != cudaSuccess) st = MOE_ERR_CUDA;
     for (int i = 0; i < nk && st == MOE_OK; ++i) {

@@ -132,14 +132,25 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 // combine runs as each output column block completes.  Counters live in the workspace's
 // sync region, which the host zeroes before the launch.
 constexpr int kDecodeMaxTokens = kSmallRouteTokens;
-// MOE_SCHEDULE_AUTO takes the fused kernel up to this many tokens (measured on the GB300: it is
-// as fast or faster than the kernel chain there on every shape of the configs)
+// MOE_SCHEDULE_AUTO takes the fused kernel for T <= 2 on every shape, and up to 16 tokens when
+// the intermediate size I is at least 1024 (measured on the GB300 over the configs' shapes:
+// with I = 640 the items of GEMM2 are five K stages long and the kernel chain wins from 4-8
+// tokens on)
 constexpr int kDecodeAutoMaxTokens = 16;
+constexpr int kDecodeAutoAlwaysTokens = 2;
+constexpr int kDecodeAutoMinI = 1024;
+
 constexpr int kDecodeMaxPairs = kDecodeMaxTokens * kMaxTopK;  // routed rows, also active experts
 constexpr int kDecodeMaxCtas = 160;                           // grid = min(SMs, this)
+constexpr int kDecodeMaxHidden = 16384;                       // H of the fused schedule (staged row)
+inline bool decode_auto(int64_t T, int H, int I) {
+  if (H > kDecodeMaxHidden) return false;
+  return T <= kDecodeAutoAlwaysTokens || (T <= kDecodeAutoMaxTokens && I >= kDecodeAutoMinI);
+}
 // sync region (uint32 words)
 constexpr int kSyncQuant = 0;                                     // tokens quantised
 constexpr int kSyncDone2 = 1;                                     // GEMM2 parts final
+constexpr int kSyncRouted = 2;                                    // tokens routed (above 11 tokens)
 constexpr int kSyncReady = 16;                                    // [active expert] GEMM1 parts final
 constexpr int kSyncTicket = kSyncReady + kDecodeMaxPairs;         // [phase][first CTA][warp] tickets
 constexpr int kSyncWords = kSyncTicket + 2 * kDecodeMaxCtas * 8;

@@ -89,7 +89,7 @@ typedef enum {
  *   MOE_SCHEDULE_CHAIN  the kernel chain: routing + sort, quantiser, GEMM1, GEMM2, combine;
  *                       each GEMM runs one CTA per 128-row x 256-column tile over the whole K;
  *                       GEMM2 rows are stored as bf16 before the combine.
- *   MOE_SCHEDULE_FUSED  T <= 64 only (else MOE_ERR_UNSUPPORTED_SHAPE): the whole layer in one
+ *   MOE_SCHEDULE_FUSED  T <= 64 and H <= 16384 only (else MOE_ERR_UNSUPPORTED_SHAPE): the whole layer in one
  *                       persistent kernel on every SM ("feat(moe): FlyDSL MegaMoE fused EP-MoE
  *                       integration", description: one fused step for dispatch + gemm1 + quant
  *                       + gemm2 + combine).  Each CTA routes and sorts the batch itself; the
@@ -97,8 +97,10 @@ typedef enum {
  *                       accumulators of an item cut between CTAs are summed in CTA order by
  *                       the last contributor (deterministic); GEMM2 rows stay fp32 up to the
  *                       combine.  Preceded by a memset of the workspace's status and sync words.
- *   MOE_SCHEDULE_AUTO   the library's choice: FUSED for T <= 16, CHAIN above (every named
- *                       entry point uses this rule).
+ *   MOE_SCHEDULE_AUTO   the library's choice (every named entry point uses this rule): FUSED
+ *                       for T <= 2, and for T <= 16 when I >= 1024 (H <= 16384 in both cases),
+ *                       CHAIN otherwise -- the faster of the two on the GB300 over the shapes
+ *                       measured (with I = 640 the chain wins from 4-8 tokens on).
  * Every schedule computes the same routing, permutation and quantised activations bit for
  * bit; outputs agree within the parity tolerance of the layer, and each schedule is
  * deterministic (repeated calls give the same bits).
@@ -339,14 +341,13 @@ moe_status_t moe_forward_ex(const moe_forward_args_t* args);
  */
 moe_status_t moe_read_device_status(const void* workspace, void* stream, moe_status_t* status_out);
 
-/* Number of kernels one forward call launches for T tokens under MOE_SCHEDULE_AUTO: 0 for
- * T = 0, 1 for T <= 16 (the fused decode kernel), 5 for T <= 64, 7 above. */
-int moe_forward_launch_count(int64_t T);
+/* Number of kernels one forward call of T tokens, hidden size H and intermediate size I
+ * launches under MOE_SCHEDULE_AUTO: 0 for T = 0, 1 when the fused kernel is chosen, else the
+ * kernel chain's 5 (T <= 64: routing and sort in one kernel) or 7. */
+int moe_forward_launch_count(int64_t T, int H, int I);
 
-/* The same for a given schedule (moe_schedule_t): the kernel chain launches 5 kernels for
- * T <= 64 (routing and sort in one kernel) and 7 above; the fused schedule 1.  Returns -1 for
- * an unknown schedule. */
-int moe_forward_launch_count_ex(int64_t T, int schedule);
+/* The same for a given schedule (moe_schedule_t); -1 for an unknown schedule. */
+int moe_forward_launch_count_ex(int64_t T, int H, int I, int schedule);
 
 /*
  * Profiling form of the forward: enqueues exactly the launch sequence of

@@ -103,15 +103,19 @@ def test_forward_validation_before_any_launch():
 
 
 def test_forward_launch_count():
-    assert moe.moe_forward_launch_count(0) == 0
-    assert moe.moe_forward_launch_count(1) == 1      # fused decode kernel
-    assert moe.moe_forward_launch_count(16) == 1
-    assert moe.moe_forward_launch_count(17) == 5     # kernel chain, routing + sort in one kernel
-    assert moe.moe_forward_launch_count(65) == 7
-    assert moe.moe_forward_launch_count_ex(64, moe.MOE_SCHEDULE_CHAIN) == 5
-    assert moe.moe_forward_launch_count_ex(65, moe.MOE_SCHEDULE_CHAIN) == 7
-    assert moe.moe_forward_launch_count_ex(3, moe.MOE_SCHEDULE_FUSED) == 1
-    assert moe.moe_forward_launch_count_ex(3, 9) == -1
+    pro, flash = (7168, 3072), (5120, 640)
+    assert moe.moe_forward_launch_count(0, *pro) == 0
+    assert moe.moe_forward_launch_count(1, *pro) == 1      # fused decode kernel
+    assert moe.moe_forward_launch_count(16, *pro) == 1
+    assert moe.moe_forward_launch_count(17, *pro) == 5     # kernel chain, routing + sort in one kernel
+    assert moe.moe_forward_launch_count(65, *pro) == 7
+    assert moe.moe_forward_launch_count(2, *flash) == 1    # small I: fused only for T <= 2
+    assert moe.moe_forward_launch_count(3, *flash) == 5
+    assert moe.moe_forward_launch_count(1, 32768, 256) == 5  # H beyond the fused kernel's staged row
+    assert moe.moe_forward_launch_count_ex(64, *pro, moe.MOE_SCHEDULE_CHAIN) == 5
+    assert moe.moe_forward_launch_count_ex(65, *pro, moe.MOE_SCHEDULE_CHAIN) == 7
+    assert moe.moe_forward_launch_count_ex(3, *flash, moe.MOE_SCHEDULE_FUSED) == 1
+    assert moe.moe_forward_launch_count_ex(3, *flash, 9) == -1
 
 
 def test_forward_ex_schedule_validation():
