@@ -76,6 +76,9 @@ def _load():
         lib.oracle_moe_forward.restype = i32
         lib.oracle_moe_forward.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, P, i64,
                                            P, P, P, P, P, i32]
+        lib.oracle_moe_forward_opts.restype = i32
+        lib.oracle_moe_forward_opts.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, P, i64,
+                                                P, P, P, P, P, i32, i32]
         lib.oracle_max_threads.restype = i32
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -188,8 +191,12 @@ def f64_to_bf16(v: float) -> int:
 
 
 def moe_forward(x_bits, logits, w1, w1s, w2, w2s, E: int, k: int, act_fmt: int, tokens=None,
-                diagnostics: bool = False, nthreads: int | None = None):
+                diagnostics: bool = False, nthreads: int | None = None, h_bf16: bool = False):
     """The whole expert layer for the listed tokens (all tokens if None).
+
+    h_bf16: round the SwiGLU output h to bf16 before its MX quantisation (the bf16-out stage-1
+    form of "[HIP] gfx950 A8W4 fused_moe configs for DSv4.1 TP-sharded experts", How the rows
+    were chosen); by default h is quantised from fp32, as the fused stage-1 epilogue does.
 
     x_bits uint16 [T, H] (bf16 bit patterns), logits fp32 [T, E],
     w1 uint8 [E, 2I, H/2], w1s uint8 [E, 2I, H/32], w2 uint8 [E, H, I/2], w2s uint8 [E, H, I/32].
@@ -219,11 +226,12 @@ def moe_forward(x_bits, logits, w1, w1s, w2, w2s, E: int, k: int, act_fmt: int, 
                     y2=np.zeros((n, k, H), np.float32))
     if nthreads is None:
         nthreads = max_threads()
-    rc = _load().oracle_moe_forward(
+    rc = _load().oracle_moe_forward_opts(
         _ptr(x_bits), _ptr(logits), _ptr(w1), _ptr(w1s), _ptr(w2), _ptr(w2s), T, H, I, E, k, act_fmt,
         _ptr(tok), n, _ptr(out),
         _ptr(diag["h"]) if diag else None, _ptr(diag["a2"]) if diag else None,
-        _ptr(diag["a2s"]) if diag else None, _ptr(diag["y2"]) if diag else None, int(nthreads))
+        _ptr(diag["a2s"]) if diag else None, _ptr(diag["y2"]) if diag else None, int(nthreads),
+        1 if h_bf16 else 0)
     if rc != 0:
         raise ValueError("oracle_moe_forward rejected its arguments")
     return (out, diag) if diagnostics else out

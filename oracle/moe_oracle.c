@@ -15,26 +15,30 @@
  *     softmax in double; the k selected probabilities renormalised to sum 1.
  *  2. Stable counting sort of the (token, slot) pairs by expert -- the local
  *     form of the dispatch step of "feat(moe): FlyDSL MegaMoE fused EP-MoE
- *     integration" (description: "dispatch+gemm1+quant+gemm2+combine"), with
- *     64-bit offsets (same page: a larger batch "overflows a stage2 int32
- *     kernel arg").
+ *     integration" (description: the expert step is dispatch, GEMM1, quant,
+ *     GEMM2, combine), with 64-bit offsets (the same page reports an int32
+ *     kernel argument overflowing on larger batches).
  *  3. MX quantisation of BF16 activations with one E8M0 scale per 1x32 block
  *     ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical
- *     Details: "quantize BF16 activations to MXFP4 with per-1x32 E8M0
- *     scales"; the same with FP8 E4M3 codes for A8W4).  Element formats and
+ *     Details: BF16 activations become MXFP4 codes with a per-1x32 E8M0
+ *     scale; the same with FP8 E4M3 codes for A8W4).  Element formats and
  *     the scale rule follow the OCP Microscaling (MX) v1.0 definitions:
  *     X = 2^(floor(log2 amax) - emax_elem), codes = RNE-satfinite(v / X).
  *  4. GEMM1 against gate/up-interleaved MXFP4 weights (row 2j = gate_j,
  *     row 2j+1 = up_j: "feat(moe): FlyDSL MegaMoE ..." description, the
  *     INTERLEAVE(g1u1) gate mode), products of decoded codes summed in
  *     double, rounded once to fp32.
- *  5. SwiGLU h_j = silu(gate_j) * up_j in fp32.
- *  6. Requantisation of h to MX (A2: "emit FP4 A2 activations/scales" for
- *     A4W4; MXFP8 for A8W4).
+ *  5. SwiGLU h_j = silu(gate_j) * up_j in fp32.  With the bf16-h option
+ *     (ORACLE_OPT_H_BF16) h is rounded to bf16 first: the bf16-out stage-1
+ *     family of "[HIP] gfx950 A8W4 fused_moe configs for DSv4.1 TP-sharded
+ *     experts" (How the rows were chosen), whose GEMM1 writes bf16 and a
+ *     separate kernel requantises.
+ *  6. Requantisation of h to MX (A2: the same page on MegaMoE has the A4W4
+ *     stage 1 produce FP4 A2 codes with their scales; MXFP8 for A8W4).
  *  7. GEMM2 (same arithmetic as 4).
- *  8. Top-k-weighted combine, accumulated in fp64 in slot order ("accumulate
- *     TopK contributions in FP32" -- the oracle uses a wider accumulator),
- *     rounded once to bf16 (round to nearest even).
+ *  8. Top-k-weighted combine, accumulated in slot order (the pages sum the
+ *     top-k contributions in FP32; the oracle uses fp64), rounded once to
+ *     bf16 (round to nearest even).
  *
  * Readings where the pages are silent (all listed in the design notes):
  *  - amax == 0 or fp32-subnormal: scale byte 0, every code a signed zero.
@@ -341,10 +345,19 @@ static float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
  *   y2_out  fp32 [n_tok, k, H]
  * Returns 0, or -1 on bad arguments.
  */
-int oracle_moe_forward(const uint16_t* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
-                       const uint8_t* w2, const uint8_t* w2s, int64_t T, int H, int I, int E, int k,
-                       int act_fmt, const int64_t* tokens, int64_t n_tok, uint16_t* out, float* h_out,
-                       uint8_t* a2_codes, uint8_t* a2_scales, float* y2_out, int nthreads) {
+#define ORACLE_OPT_H_BF16 1 /* round h to bf16 (nearest even) before its MX quantisation */
+
+static float round_bf16(float v) {
+  const uint32_t bits = (uint32_t)f64_to_bf16_rne((double)v) << 16;
+  float r;
+  memcpy(&r, &bits, sizeof(r));
+  return r;
+}
+
+int oracle_moe_forward_opts(const uint16_t* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
+                            const uint8_t* w2, const uint8_t* w2s, int64_t T, int H, int I, int E, int k,
+                            int act_fmt, const int64_t* tokens, int64_t n_tok, uint16_t* out, float* h_out,
+                            uint8_t* a2_codes, uint8_t* a2_scales, float* y2_out, int nthreads, int opts) {
   if (H % 32 || I % 32 || k < 1 || k > 64 || k > E || T < 0) return -1;
   if (act_fmt != ORACLE_FMT_E4M3 && act_fmt != ORACLE_FMT_E2M1) return -1;
   if (!e4m3_ready) e4m3_build();
@@ -390,6 +403,7 @@ int oracle_moe_forward(const uint16_t* x, const float* logits, const uint8_t* w1
           g_up[half] = (float)s;
         }
         h[i] = silu_mul(g_up[0], g_up[1]);
+        if (opts & ORACLE_OPT_H_BF16) h[i] = round_bf16(h[i]);
       }
       /* 6. A2 */
       oracle_quantize_rows_f32(h, 1, I, act_fmt, a2, a2s);
@@ -412,6 +426,15 @@ int oracle_moe_forward(const uint16_t* x, const float* logits, const uint8_t* w1
     free(xq); free(xs); free(xd); free(acc); free(h); free(a2); free(a2s); free(a2d);
   }
   return 0;
+}
+
+/* The layer as the method defines it (h quantised from fp32). */
+int oracle_moe_forward(const uint16_t* x, const float* logits, const uint8_t* w1, const uint8_t* w1s,
+                       const uint8_t* w2, const uint8_t* w2s, int64_t T, int H, int I, int E, int k,
+                       int act_fmt, const int64_t* tokens, int64_t n_tok, uint16_t* out, float* h_out,
+                       uint8_t* a2_codes, uint8_t* a2_scales, float* y2_out, int nthreads) {
+  return oracle_moe_forward_opts(x, logits, w1, w1s, w2, w2s, T, H, I, E, k, act_fmt, tokens, n_tok, out, h_out,
+                                 a2_codes, a2_scales, y2_out, nthreads, 0);
 }
 
 int oracle_max_threads(void) {

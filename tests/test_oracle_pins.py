@@ -294,9 +294,10 @@ def _tiny_case(T=16, H=256, I=128, E=8, k=2, seed=0, act=E4M3):
                 w1b=w1b, w2b=w2b)
 
 
-def _dense_masked(c):
+def _dense_masked(c, h_bf16=False):
     """Brute force over ALL experts for every token, masked by the routing:
-    no sort, no gather, numpy matmuls, the numpy MX restatement, torch softmax."""
+    no sort, no gather, numpy matmuls, the numpy MX restatement, torch softmax.
+    h_bf16: h rounded to bf16 (numpy round-to-nearest-even) before its quantisation."""
     T, H, I, E, k, act = c["T"], c["H"], c["I"], c["E"], c["k"], c["act"]
     x = mx_ref.bf16_bits_to_f64(c["x"]).astype(np.float32)
     xq, _ = mx_ref.quantize_values(x, act)
@@ -313,20 +314,41 @@ def _dense_masked(c):
         acc = (xq @ W1[e].T).astype(np.float32)  # [T, 2I]
         g, u = acc[:, 0::2], acc[:, 1::2]
         h = (g / (np.float32(1) + np.exp(-g)) * u).astype(np.float32)
+        if h_bf16:
+            h = mx_ref.bf16_rne(h.astype(np.float64)).astype(np.float32)
         a2, _ = mx_ref.quantize_values(h, act)
         y2 = (a2 @ W2[e].T).astype(np.float32).astype(np.float64)
         out += mask[:, e:e + 1].astype(np.float32).astype(np.float64) * y2
     return out
 
 
+@pytest.mark.parametrize("h_bf16", [False, True])
 @pytest.mark.parametrize("act", [E4M3, E2M1])
-def test_forward_equals_dense_masked_brute_force(act):
+def test_forward_equals_dense_masked_brute_force(act, h_bf16):
     c = _tiny_case(act=act)
     got = mx_ref.bf16_bits_to_f64(oracle.moe_forward(c["x"], c["lg"], c["w1"], c["w1s"], c["w2"], c["w2s"],
-                                                     c["E"], c["k"], act))
-    want = _dense_masked(c)
+                                                     c["E"], c["k"], act, h_bf16=h_bf16))
+    want = _dense_masked(c, h_bf16)
     ulp = np.ldexp(1.0, np.frexp(np.abs(want) + 1e-30)[1] - 8)
     assert np.all(np.abs(got - want) <= ulp), np.abs(got - want).max()
+
+
+@pytest.mark.parametrize("act", [E4M3, E2M1])
+def test_h_bf16_option_rounds_h_and_requantises_it(act):
+    """With h rounded to bf16, the diagnostics' h is the fp32 run's h rounded to nearest even,
+    and A2 is the oracle's row quantiser applied to that h; the output moves by the re-rounding
+    of a few percent of the A2 codes (a code step across a rounding boundary)."""
+    c = _tiny_case(act=act)
+    args = (c["x"], c["lg"], c["w1"], c["w1s"], c["w2"], c["w2s"], c["E"], c["k"], act)
+    out32, d32 = oracle.moe_forward(*args, diagnostics=True)
+    out16, d16 = oracle.moe_forward(*args, diagnostics=True, h_bf16=True)
+    assert np.array_equal(d16["h"], mx_ref.bf16_rne(d32["h"].astype(np.float64)).astype(np.float32))
+    codes, scales = oracle.quantize_rows_f32(d16["h"].reshape(-1, c["I"]), act)
+    assert np.array_equal(codes.reshape(d16["a2"].shape), d16["a2"])
+    assert np.array_equal(scales.reshape(d16["a2s"].shape), d16["a2s"])
+    a, b = mx_ref.bf16_bits_to_f64(out16), mx_ref.bf16_bits_to_f64(out32)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 0 < rel < 0.1, rel
 
 
 def test_forward_token_subset_equals_full_rows():
