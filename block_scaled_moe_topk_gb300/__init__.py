@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "MOE_SCHEDULE_AUTO", "MOE_SCHEDULE_CHAIN", "MOE_SCHEDULE_FUSED",
-    "lib", "moe_status_string", "moe_workspace_bytes",
+    "MOE_SCHEDULE_CHAIN_BF16_H", "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
     "moe_quantize_mx", "moe_a8w4_forward",
     "moe_a4w4_forward", "moe_forward_ex", "moe_a8w4_forward_prequant", "moe_a4w4_forward_prequant", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
@@ -28,6 +28,7 @@ MOE_ACT_MXFP4 = 1
 MOE_SCHEDULE_AUTO = 0   # the library's choice for the shape and T
 MOE_SCHEDULE_CHAIN = 1  # kernel chain, one CTA per 128 x 256 GEMM tile over the whole K
 MOE_SCHEDULE_FUSED = 2  # T <= 64: the whole layer in one persistent kernel
+MOE_SCHEDULE_CHAIN_BF16_H = 3  # kernel chain, GEMM1 writes bf16 h, a separate kernel requantises
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_topk.so")
 
 STATUS_NAMES = {
@@ -259,6 +260,8 @@ def moe_a4w4_forward_prepacked(x, gate_logits, w1, w1_scale_tiled, w2, w2_scale_
 KERNEL_NAMES = ("route", "scan", "scatter", "quant", "gemm1", "gemm2", "combine")
 KERNEL_NAMES_SMALL = ("route_sort", "quant", "gemm1", "gemm2", "combine")  # kernel chain, T <= 64
 KERNEL_NAMES_FUSED = ("decode",)  # fused schedule
+KERNEL_NAMES_BF16_H = ("route", "scan", "scatter", "quant", "gemm1", "requant", "gemm2", "combine")
+KERNEL_NAMES_BF16_H_SMALL = ("route_sort", "quant", "gemm1", "requant", "gemm2", "combine")
 
 
 def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E, k, workspace, stream=None,
@@ -273,8 +276,11 @@ def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E,
                                      workspace.numel() * workspace.element_size(), _stream(stream),
                                      int(bool(prepacked_scales)), int(schedule), us),
            "moe_profile_forward")
-    names = {len(KERNEL_NAMES): KERNEL_NAMES, len(KERNEL_NAMES_SMALL): KERNEL_NAMES_SMALL,
-             1: KERNEL_NAMES_FUSED}[n]
+    if schedule == MOE_SCHEDULE_CHAIN_BF16_H:
+        names = KERNEL_NAMES_BF16_H if n == len(KERNEL_NAMES_BF16_H) else KERNEL_NAMES_BF16_H_SMALL
+    else:
+        names = {len(KERNEL_NAMES): KERNEL_NAMES, len(KERNEL_NAMES_SMALL): KERNEL_NAMES_SMALL,
+                 1: KERNEL_NAMES_FUSED}[n]
     return {names[i]: float(us[i]) for i in range(n)}
 
 

@@ -480,6 +480,11 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
   // a_rows = 16: no tile has more routed rows; 64: 64-row work units (any routing); else 128.
   // A4W4's larger stages gain no extra stage from a 64-row slot.
+  if (a.epilogue == 2) {  // GEMM1 writing bf16 h (the bf16-out form)
+    if (a.a_rows <= 16) return a.act_fmt == 0 ? launch_typed<0, 2, 16>(a, s) : launch_typed<1, 2, 16>(a, s);
+    if (a.a_rows <= 64 && a.act_fmt == 0) return launch_typed<0, 2, 64>(a, s);
+    return a.act_fmt == 0 ? launch_typed<0, 2, kRowTile>(a, s) : launch_typed<1, 2, kRowTile>(a, s);
+  }
   if (a.a_rows <= 16) {
     if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, 16>(a, s) : launch_typed<0, 1, 16>(a, s);
     return a.epilogue == 0 ? launch_typed<1, 0, 16>(a, s) : launch_typed<1, 1, 16>(a, s);

@@ -139,6 +139,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 //                  (ACT 1) codes into out_codes [rows, N/2 or N/4] and one E8M0 byte per block
 //                  into out_sf (128x4 tile layout over N/2 columns).
 //   EPI 1 (GEMM2): the fp32 row rounded to bf16 (nearest even) into out_bf16 [rows, N].
+//   EPI 2 (GEMM1, bf16-out form): h_j = silu(gate_j) * up_j rounded to bf16 into out_bf16
+//                  [rows, N/2], for a separate requantisation kernel.
 template <int ACT, int EPI>
 __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, int64_t prow, int nt, int half, int N,
                                                uint8_t* out_codes, uint8_t* out_sf, uint16_t* out_bf16) {
@@ -177,6 +179,22 @@ __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, in
         }
         out_sf[sf_tile_offset(prow, kb, I)] = sc.byte;
       }
+    }
+  } else if (EPI == 2) {
+    if (!valid) return;  // padding rows: nothing stored (and no SwiGLU on their stale values)
+    const int I = N / 2;
+    uint4* d4 = reinterpret_cast<uint4*>(out_bf16 + prow * I + nt * (kNTile / 2) + half * 64);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t w[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j = 8 * i + 2 * c;  // h columns j, j + 1 of this thread's 64
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(silu_mul(acc[2 * j], acc[2 * j + 1]),
+                                                        silu_mul(acc[2 * j + 2], acc[2 * j + 3]));
+        w[c] = *reinterpret_cast<const uint32_t*>(&hb);
+      }
+      d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else if (valid) {
     uint4* d4 = reinterpret_cast<uint4*>(out_bf16 + prow * N + nt * kNTile + half * 128);

@@ -140,13 +140,19 @@ int test_stall_producer() {
 // Kernel chain, T > 64: route, scan, scatter, quant, gemm1, gemm2, combine; T <= 64:
 // route_sort, quant, gemm1, gemm2, combine.  Fused schedule (T <= 64): one decode kernel.
 constexpr int kForwardKernels = 7;
+constexpr int kMaxForwardKernels = 8;  // the chain with the bf16-out GEMM1 and its requant kernel
+bool valid_schedule(int schedule) {
+  return schedule == MOE_SCHEDULE_AUTO || schedule == MOE_SCHEDULE_CHAIN || schedule == MOE_SCHEDULE_FUSED ||
+         schedule == MOE_SCHEDULE_CHAIN_BF16_H;
+}
 bool use_fused(int64_t T, int schedule, int H, int I) {
   return schedule == MOE_SCHEDULE_FUSED || (schedule == MOE_SCHEDULE_AUTO && moe::decode_auto(T, H, I));
 }
 int launch_count(int64_t T, int H, int I, int schedule = MOE_SCHEDULE_AUTO) {
   if (T <= 0) return 0;
   if (use_fused(T, schedule, H, I)) return 1;
-  return T <= moe::kSmallRouteTokens ? 5 : kForwardKernels;
+  const int requant = schedule == MOE_SCHEDULE_CHAIN_BF16_H ? 1 : 0;  // the separate requant kernel
+  return (T <= moe::kSmallRouteTokens ? 5 : kForwardKernels) + requant;
 }
 
 // x is bf16 [T, H] when x_scale is null, else prequantised codes [T, H or H/2] with canonical
@@ -164,8 +170,10 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
       !aligned(w1s, tiled_scales ? 16 : 4) || !aligned(w2s, tiled_scales ? 16 : 4) || !aligned(ws, 256))
     return MOE_ERR_MISALIGNED;
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN && schedule != MOE_SCHEDULE_FUSED)
-    return MOE_ERR_INVALID_ARG;
+  if (!valid_schedule(schedule)) return MOE_ERR_INVALID_ARG;
+  // the bf16-out GEMM1 keeps h in the y2 region (rows_cap x H bf16), requantised by a kernel of
+  // at most 1024 threads of 16 elements
+  if (schedule == MOE_SCHEDULE_CHAIN_BF16_H && (I > H || I > 16384)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (schedule == MOE_SCHEDULE_FUSED && (T > moe::kDecodeMaxTokens || H > moe::kDecodeMaxHidden))
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
@@ -291,8 +299,23 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
     return few_rows && K / 128 >= moe::kUnit64MinStages ? 64 : kRowTile;
   };
   g1.a_rows = a_rows_for(H);
+  const bool bf16_h = schedule == MOE_SCHEDULE_CHAIN_BF16_H;
+  if (bf16_h) {
+    // GEMM1 leaves h = SwiGLU(acc) as bf16 rows in the y2 region; a separate kernel requantises
+    // the routed rows into A2 (GEMM2 overwrites the region with y2 afterwards)
+    g1.epilogue = 2;
+    g1.out_codes = nullptr;
+    g1.out_sf = nullptr;
+    g1.out_bf16 = reinterpret_cast<uint16_t*>(at(L.y2));
+  }
   MOE_CUDA_TRY(moe::launch_gemm(g1, s));
   MOE_CUDA_TRY(mark());
+  if (bf16_h) {
+    moe::RequantArgs rq{reinterpret_cast<const uint16_t*>(at(L.y2)), inv_padded, T * (int64_t)k, I, afmt, at(L.a2),
+                        at(L.a2s)};
+    MOE_CUDA_TRY(moe::launch_requant(rq, s));
+    MOE_CUDA_TRY(mark());
+  }
 
   moe::GemmArgs g2 = g1;
   g2.epilogue = 1;
@@ -482,7 +505,7 @@ moe_status_t moe_read_device_status(const void* ws, void* stream, moe_status_t* 
 int moe_forward_launch_count(int64_t T, int H, int I) { return launch_count(T, H, I); }
 
 int moe_forward_launch_count_ex(int64_t T, int H, int I, int schedule) {
-  if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_CHAIN && schedule != MOE_SCHEDULE_FUSED) return -1;
+  if (!valid_schedule(schedule)) return -1;
   return launch_count(T, H, I, schedule);
 }
 
@@ -492,9 +515,9 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* 
                                  int prepacked_scales, int schedule, float* kernel_us) {
   if (!kernel_us) return MOE_ERR_INVALID_ARG;
   if (fmt != MOE_ACT_MXFP8 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
-  cudaEvent_t ev[kForwardKernels + 1] = {};
+  cudaEvent_t ev[kMaxForwardKernels + 1] = {};
   moe_status_t st = MOE_OK;
-  for (int i = 0; i <= kForwardKernels && st == MOE_OK; ++i)
+  for (int i = 0; i <= kMaxForwardKernels && st == MOE_OK; ++i)
     if (cudaEventCreate(&ev[i]) != cudaSuccess) st = MOE_ERR_CUDA;
   if (st == MOE_OK)
     st = forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt,
@@ -508,7 +531,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* 
       kernel_us[i] = ms * 1000.0f;
     }
   }
-  for (int i = 0; i <= kForwardKernels; ++i)
+  for (int i = 0; i <= kMaxForwardKernels; ++i)
     if (ev[i]) cudaEventDestroy(ev[i]);
   return st;
 }

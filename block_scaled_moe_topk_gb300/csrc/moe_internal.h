@@ -89,13 +89,26 @@ struct PermuteArgs {
   uint8_t* scales_out;
 };
 cudaError_t launch_permute_rows(const PermuteArgs& a, cudaStream_t s);
+// bf16 rows h [rows_cap, K] at the padded rows inv_padded[q] of the R routed pairs -> MX codes
+// of the same rows (E4M3 or E2M1) and their scales in the 128x4 tile layout (K % 128 == 0).
+struct RequantArgs {
+  const uint16_t* h;
+  const int32_t* inv_padded;
+  int64_t R;
+  int K;
+  int fmt;
+  uint8_t* codes;
+  uint8_t* scales;
+};
+cudaError_t launch_requant(const RequantArgs& a, cudaStream_t s);
 // Canonical [rows, K/32] scales -> 128x4 tile layout (rows % 128 == 0, K % 128 == 0).
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst, cudaStream_t s);
 
 // gemm.cu
 struct GemmArgs {
   int act_fmt;            // 0: E4M3 activations (kind::mxf8f6f4), 1: E2M1 (kind::mxf4)
-  int epilogue;           // 0: SwiGLU + MX requant (GEMM1), 1: fp32 rows (GEMM2)
+  int epilogue;           // 0: SwiGLU + MX requant (GEMM1), 1: bf16 rows (GEMM2), 2: bf16 SwiGLU
+                          // rows h [rows_cap, N/2] into out_bf16 (GEMM1, bf16-out form)
   const uint8_t* act;     // activation codes [rows_cap, K or K/2]
   const uint8_t* act_sf;  // [rows_cap/128][K/128][512]
   int64_t rows_cap;

@@ -144,6 +144,45 @@ __global__ void __launch_bounds__(1024) quant_rows_kernel(QuantArgs a) {
   }
 }
 
+// Requantisation of the bf16-out GEMM1 form: one block per routed pair q, thread i owns
+// elements [16i, 16i + 16) of the row's h; the codes and scales go to the same padded row.
+template <int FMT>
+__global__ void __launch_bounds__(1024) requant_rows_kernel(RequantArgs a) {
+  const int K = a.K;
+  const int64_t prow = a.inv_padded[blockIdx.x];
+  const int col0 = (int)threadIdx.x * 16;
+  const bool active = col0 < K;
+  float v[16];
+  if (active) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.h + prow * K + col0);
+    const uint4 r0 = src[0], r1 = src[1];
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = 0.0f;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  if (!active) return;
+  const MxScale sc = mx_scale<FMT>(amax);
+  const int kb = col0 / 32;
+  if (FMT == 0) {
+    const uint2 c0 = pack_e4m3x8(v, sc.mult), c1 = pack_e4m3x8(v + 8, sc.mult);
+    *reinterpret_cast<uint4*>(a.codes + prow * K + col0) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+  } else {
+    *reinterpret_cast<uint2*>(a.codes + prow * (K / 2) + col0 / 2) =
+        make_uint2(pack_e2m1x8(v, sc.mult), pack_e2m1x8(v + 8, sc.mult));
+  }
+  if ((col0 & 31) == 0) a.scales[sf_tile_offset(prow, kb, K)] = sc.byte;
+}
+
 // Canonical E8M0 scales [rows, K/32] -> the 128x4 tile layout the GEMM copies to TMEM:
 // thread i moves the 4 scale bytes (one 128-wide k-atom) of one row.
 __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* src, int64_t rows, int K, uint8_t* dst) {
@@ -186,6 +225,15 @@ cudaError_t launch_permute_rows(const PermuteArgs& a, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
   permute_rows_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_requant(const RequantArgs& a, cudaStream_t s) {
+  if (a.R == 0) return cudaSuccess;
+  if (a.K > 16 * 1024 || a.R > 0x7fffffff) return cudaErrorInvalidValue;
+  const unsigned threads = (unsigned)((a.K / 16 + 31) / 32 * 32);
+  if (a.fmt == 0) requant_rows_kernel<0><<<(unsigned)a.R, threads, 0, s>>>(a);
+  else requant_rows_kernel<1><<<(unsigned)a.R, threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,14 @@ typedef enum {
  *                       accumulators of an item cut between CTAs are summed in CTA order by
  *                       the last contributor (deterministic); GEMM2 rows stay fp32 up to the
  *                       combine.  Preceded by a memset of the workspace's status and sync words.
+ *   MOE_SCHEDULE_CHAIN_BF16_H  the kernel chain with GEMM1 in its bf16-out form: the GEMM1
+ *                       epilogue writes h = SwiGLU(acc) as bf16 rows and a separate kernel
+ *                       requantises them into A2 ("[HIP] gfx950 A8W4 fused_moe configs for
+ *                       DSv4.1 TP-sharded experts", How the rows were chosen: the bf16-out stage-1
+ *                       family against the fused-quant one).  h is rounded to bf16 before its MX
+ *                       quantisation, so A2 can differ from the fused epilogue's in a few codes.
+ *                       Needs I <= H and I <= 16384 (h is kept in the y2 region), else
+ *                       MOE_ERR_UNSUPPORTED_SHAPE.  One kernel more than CHAIN.
  *   MOE_SCHEDULE_AUTO   the library's choice (every named entry point uses this rule): FUSED
  *                       for T <= 2, and for T <= 16 when I >= 1024 (H <= 16384 in both cases),
  *                       CHAIN otherwise -- the faster of the two on the GB300 over the shapes
@@ -108,7 +116,8 @@ typedef enum {
 typedef enum {
   MOE_SCHEDULE_AUTO = 0,
   MOE_SCHEDULE_CHAIN = 1,
-  MOE_SCHEDULE_FUSED = 2
+  MOE_SCHEDULE_FUSED = 2,
+  MOE_SCHEDULE_CHAIN_BF16_H = 3
 } moe_schedule_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -358,7 +367,8 @@ int moe_forward_launch_count_ex(int64_t T, int H, int I, int schedule);
  * waits for the last event, and writes the duration of each kernel in
  * microseconds to kernel_us[moe_forward_launch_count_ex(T, schedule)] (HOST array),
  * in launch order: route, scan, scatter, quant, gemm1, gemm2, combine (chain, T > 64),
- * route_sort, quant, gemm1, gemm2, combine (chain, T <= 64) or decode (fused).
+ * route_sort, quant, gemm1, gemm2, combine (chain, T <= 64) or decode (fused); the bf16-out
+ * chain adds requant after gemm1.
  * Arguments and errors as for the forward; additionally synchronises on its
  * own events (so it is not graph-capturable) and creates/destroys them.
  */

@@ -116,6 +116,8 @@ def test_forward_launch_count():
     assert moe.moe_forward_launch_count_ex(65, *pro, moe.MOE_SCHEDULE_CHAIN) == 7
     assert moe.moe_forward_launch_count_ex(3, *flash, moe.MOE_SCHEDULE_FUSED) == 1
     assert moe.moe_forward_launch_count_ex(3, *flash, 9) == -1
+    assert moe.moe_forward_launch_count_ex(3, *flash, moe.MOE_SCHEDULE_CHAIN_BF16_H) == 6
+    assert moe.moe_forward_launch_count_ex(100, *pro, moe.MOE_SCHEDULE_CHAIN_BF16_H) == 8
 
 
 def test_forward_ex_schedule_validation():
@@ -127,6 +129,11 @@ def test_forward_ex_schedule_validation():
     assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 1
     a.schedule = -1
     assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 1
+    a.schedule = moe.MOE_SCHEDULE_CHAIN_BF16_H
+    a.I = 512  # h lives in the y2 region: I <= H
+    a.workspace_bytes = moe.moe_workspace_bytes(16, 256, 512, 8, 2)
+    assert moe.lib().moe_forward_ex(ctypes.byref(a)) == 2
+    a.I = 128
     a.schedule = moe.MOE_SCHEDULE_FUSED
     a.T = 65  # the fused schedule takes at most 64 tokens
     a.workspace_bytes = moe.moe_workspace_bytes(65, 256, 128, 8, 2)

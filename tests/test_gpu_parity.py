@@ -645,8 +645,47 @@ def test_profile_forward_fused():
     out_a = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
     out_b = torch.empty_like(out_a)
     ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
-    moe.moe_a8w4_forward(x, lg, *W.dev, out_a, s.E, s.k, ws)
-    us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws)
+    moe.moe_forward_ex(x, lg, *W.dev, out_a, s.E, s.k, ws, schedule=moe.MOE_SCHEDULE_FUSED)
+    us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws,
+                                 schedule=moe.MOE_SCHEDULE_FUSED)
     torch.cuda.synchronize()
     assert list(us) == ["decode"] and us["decode"] > 0
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+# --------------------------------------------------------------------------- bf16-out GEMM1 form
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("shape,T", [("tiny", 16), ("flash_decode", 1), ("flash_decode", 64), ("draft", 300),
+                                     ("flash_tp2", 1000)])
+def test_chain_bf16_h_against_oracle(act, shape, T):
+    """GEMM1 writing h as bf16 and a separate requant kernel (the pages' bf16-out stage-1
+    family) against the oracle with h rounded to bf16 the same way: output within the parity
+    tolerance; A2 codes within a small mismatch rate (GEMM1's fp32 accumulation against the
+    oracle's fp64 moves a few h values across a bf16 rounding boundary)."""
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 11), synth.gate_logits(T, s.E, 11, skew=s.skew)
+    out, ws = _run_forward(act, x, lg, W, s.E, s.k, schedule=moe.MOE_SCHEDULE_CHAIN_BF16_H)
+    toks = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(T).choice(T, 48, replace=False))
+    v, inv_p = _check_intermediates(act, x, lg, W, s.E, s.k, ws, tokens=toks)
+    want, diag = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, act, tokens=toks,
+                                    diagnostics=True, h_bf16=True)
+    assert _a2_mismatch(act, v, inv_p, diag, toks, s.k, s.I) < 0.02
+    rel, cos = compare(bits(out)[toks], want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+def test_profile_forward_chain_bf16_h():
+    s = synth.SHAPES["flash_decode"]
+    W = _weights(s)
+    for T, names in ((4, moe.KERNEL_NAMES_BF16_H_SMALL), (100, moe.KERNEL_NAMES_BF16_H)):
+        x, lg = synth.x_bf16(T, s.H, 0).to(DEV), synth.gate_logits(T, s.E, 0).to(DEV)
+        out_a = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+        out_b = torch.empty_like(out_a)
+        ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
+        moe.moe_forward_ex(x, lg, *W.dev, out_a, s.E, s.k, ws, schedule=moe.MOE_SCHEDULE_CHAIN_BF16_H)
+        us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev, out_b, s.E, s.k, ws,
+                                     schedule=moe.MOE_SCHEDULE_CHAIN_BF16_H)
+        torch.cuda.synchronize()
+        assert list(us) == list(names) and all(v > 0 for v in us.values())
+        assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
