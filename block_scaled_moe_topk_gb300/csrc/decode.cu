@@ -770,11 +770,13 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
         const uint8_t v = stage_sf[kb];
         for (int j = 0; j < k; ++j) p.xs[sf_tile_offset(pair_invp[b * k + j], kb, H)] = v;
       }
-      __threadfence();
     }
+    // the warps' copies are ordered before the signal by the barrier and one gpu-scope fence of
+    // the signalling thread (the usual last-arriver pattern)
     named_barrier(2, 32 * kDEpiWarps);
     if (et == 0) {
       if (b < T && routed) {
+        __threadfence();
         fence_proxy_async_global();  // the codes are read by other CTAs' TMA loads
         atomicAdd(p.sync + kSyncQuant, 1u);
       }
