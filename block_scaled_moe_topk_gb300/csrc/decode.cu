@@ -683,8 +683,10 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
         if (armed[s] >= 0) lane_wait(full_bar(s), (uint32_t)armed[s], sync, 100000000ull, true);
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (lane 0)
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer: the warp runs the
+    // loop converged, one elected lane issues each tcgen05 instruction (from one divergent
+    // lane the loop itself outlasted the stage's MMAs)
+    {
       int slot = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
@@ -697,14 +699,14 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
       const bool gathered = !p.w_sf_tiled;
       MOE_FOR_EACH_SEGMENT({
         if (!ok) break;
-        if (!lane_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
+        if (!warp_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int K = P.K;
         for (int ks = ks0; ks < ks1; ++ks) {
-          if (!lane_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
+          if (!warp_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -715,29 +717,32 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
           const int kvalid = min(KPS, K - ks * KPS);
           const int katoms = kvalid == KPS ? kAtomsPerStage : kvalid / 128;
           const int nmma = kvalid == KPS ? kMmaPerStage : kvalid / TR::kMmaK;
+          if (elect_one()) {
 #pragma unroll
-          for (int ka = 0; ka < kAtomsPerStage; ++ka) {
-            if (ka < katoms) {
-              tc_cp_32x128b_warpx4(sf_col + ka * 4, sfa_desc0 + so + ka * 32);
-              tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8, sfb_desc0 + so + ka * 32);
-              tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8 + 4, sfb_desc0 + so + kHalfStep + ka * 32);
+            for (int ka = 0; ka < kAtomsPerStage; ++ka) {
+              if (ka < katoms) {
+                tc_cp_32x128b_warpx4(sf_col + ka * 4, sfa_desc0 + so + ka * 32);
+                tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8, sfb_desc0 + so + ka * 32);
+                tc_cp_32x128b_warpx4(sf_col + kSfaCols + ka * 8 + 4, sfb_desc0 + so + kHalfStep + ka * 32);
+              }
             }
-          }
 #pragma unroll
-          for (int j = 0; j < kMmaPerStage; ++j) {
-            if (j < nmma) {
-              const int kblk = j * (TR::kMmaK / 32);
-              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3), kRowTile);
-              const uint32_t acc = (ks > ks0 || j > 0) ? 1u : 0u;
-              if (ACT == 0)
-                tc_mma_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
-                                sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * 8, acc);
-              else
-                tc_mma_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, sf_col + (kblk >> 2) * 4,
-                            sf_col + kSfaCols + (kblk >> 2) * 8, acc);
+            for (int j = 0; j < kMmaPerStage; ++j) {
+              if (j < nmma) {
+                const int kblk = j * (TR::kMmaK / 32);
+                const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3), kRowTile);
+                const uint32_t acc = (ks > ks0 || j > 0) ? 1u : 0u;
+                if (ACT == 0)
+                  tc_mma_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
+                                  sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * 8, acc);
+                else
+                  tc_mma_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, sf_col + (kblk >> 2) * 4,
+                              sf_col + kSfaCols + (kblk >> 2) * 8, acc);
+              }
             }
+            tc_commit(empty_bar(slot));
           }
-          tc_commit(empty_bar(slot));
+          __syncwarp();
           issued = true;
           if (++slot == kStages) {
             slot = 0;
@@ -745,12 +750,14 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
           }
         }
         if (!ok) break;
-        tc_commit(tmem_full_bar);
+        if (elect_one()) tc_commit(tmem_full_bar);
+        __syncwarp();
         acc_phase ^= 1u;
       })
       if (issued) {
-        tc_commit(drain_bar);
-        lane_wait(drain_bar, 0, sync, 100000000ull, true);
+        if (elect_one()) tc_commit(drain_bar);
+        __syncwarp();
+        warp_wait(drain_bar, 0, sync, 100000000ull, true);
       }
     }
     __syncwarp();

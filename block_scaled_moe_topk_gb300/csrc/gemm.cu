@@ -15,10 +15,10 @@
 //   warp 10     producer: with canonical weight scales, 4-byte cp.async copies that rearrange
 //               them into that layout; with prepacked scales, the TMA of the weight tile and
 //               the bulk copies of its scales (so the two halves of a stage issue in parallel);
-//   warp 1      TMEM owner; its lane 0 issues tcgen05.cp of the scales to TMEM, then
-//               tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1, scale_vec 1X) or kind::mxf4 (E2M1 x E2M1,
-//               scale_vec 2X) into a 128x256 fp32 accumulator in TMEM, from precomputed
-//               descriptors (the issuing thread's instruction stream bounds the stage rate);
+//   warp 1      TMEM owner; converged, with one elected lane issuing tcgen05.cp of the scales
+//               to TMEM, then tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1, scale_vec 1X) or
+//               kind::mxf4 (E2M1 x E2M1, scale_vec 2X) into a 128x256 fp32 accumulator in
+//               TMEM, from precomputed descriptors;
 //   warps 2..9  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one routed row) per
 //               thread; warps 2-5 take columns [0, 128), warps 6-9 columns [128, 256).  Each
 //               thread pulls its 128 columns into registers, releases TMEM at once, and only
@@ -262,46 +262,47 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       for (int s = 0; s < kStages; ++s)
         if (armed_parity[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed_parity[s], sync, 100000000ull, true);
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer (lane 0)
-    // tcgen05.cp / tcgen05.mma / tcgen05.commit are single-thread instructions: the loop runs
-    // on one lane with its descriptors precomputed, so the issuing thread's own instruction
-    // stream stays short between stages.
-    if (lane == 0) {
-      int slot = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true, issued = false;
-      // descriptors of slot 0; a slot adds kStageBytes, an MMA step 32 bytes (start address
-      // field, in 16-byte units; shared-memory offsets stay below 2^18, so no carry)
-      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kLayoutSwizzle128B);
-      const uint64_t b_desc0 = smem_desc(sbase + G::kBOff, 16, 1024, kLayoutSwizzle128B);
-      const uint64_t sfa_desc0 = smem_desc(sbase + kSfaOff, 128, 128, kLayoutNone);
-      const uint64_t sfb_desc0 = smem_desc(sbase + kSfbOff, 128, 128, kLayoutNone);
-      constexpr uint64_t kSlotStep = kStageBytes >> 4;
-      constexpr uint32_t kHalfStep = (kAtomsPerStage * 512) >> 4;  // second 128 weight rows
-      const bool gathered = !p.w_sf_tiled;
-      for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        // A 64-row unit over rows 64..127 of its 128-row block: the block's scale tile lands in
-        // TMEM as a whole and row m reads lane m, column sfa + m/32, so the unit's rows 0..63
-        // take the scales of block rows 64..127 two columns further on.
-        uint32_t sfa_shift = 0;
-        if (G::kUnitRows == 64) sfa_shift = 2u * (uint32_t)(decode_tile(tile, unit_base, p.E, NT).mt & 1);
-        if (!lane_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
+    // ------------------------------------------------------------------ MMA issuer
+    // The warp runs the loop converged (waits, descriptor arithmetic) and one elected lane
+    // issues each tcgen05.cp / tcgen05.mma / tcgen05.commit.  From one divergent lane the same
+    // loop took longer per stage than the four MMAs it issues (the pipe then idled between
+    // stages); from the converged warp the stage runs at the MMAs' own rate.
+    int slot = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued = false;
+    // descriptors of slot 0; a slot adds kStageBytes, an MMA step 32 bytes (start address
+    // field, in 16-byte units; shared-memory offsets stay below 2^18, so no carry)
+    const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kLayoutSwizzle128B);
+    const uint64_t b_desc0 = smem_desc(sbase + G::kBOff, 16, 1024, kLayoutSwizzle128B);
+    const uint64_t sfa_desc0 = smem_desc(sbase + kSfaOff, 128, 128, kLayoutNone);
+    const uint64_t sfb_desc0 = smem_desc(sbase + kSfbOff, 128, 128, kLayoutNone);
+    constexpr uint64_t kSlotStep = kStageBytes >> 4;
+    constexpr uint32_t kHalfStep = (kAtomsPerStage * 512) >> 4;  // second 128 weight rows
+    const bool gathered = !p.w_sf_tiled;
+    for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      // A 64-row unit over rows 64..127 of its 128-row block: the block's scale tile lands in
+      // TMEM as a whole and row m reads lane m, column sfa + m/32, so the unit's rows 0..63
+      // take the scales of block rows 64..127 two columns further on.
+      uint32_t sfa_shift = 0;
+      if (G::kUnitRows == 64) sfa_shift = 2u * (uint32_t)(decode_tile(tile, unit_base, p.E, NT).mt & 1);
+      if (!warp_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!warp_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < nks; ++ks) {
-          if (!lane_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (gathered) fence_proxy_async_smem();  // scales written by cp.async, read by tcgen05.cp
-          const uint64_t so = (uint64_t)slot * kSlotStep;
-          const uint32_t sf_col = tmem_base + kSfCol0 + (uint32_t)slot * kSfSlotCols;
-          const int kvalid = min(TR::kKPerStage, K - ks * TR::kKPerStage);
-          const int katoms = kvalid == TR::kKPerStage ? kAtomsPerStage : kvalid / 128;
-          const int nmma = kvalid == TR::kKPerStage ? kMmaPerStage : kvalid / TR::kMmaK;
+        if (gathered) fence_proxy_async_smem();  // scales written by cp.async, read by tcgen05.cp
+        const uint64_t so = (uint64_t)slot * kSlotStep;
+        const uint32_t sf_col = tmem_base + kSfCol0 + (uint32_t)slot * kSfSlotCols;
+        const int kvalid = min(TR::kKPerStage, K - ks * TR::kKPerStage);
+        const int katoms = kvalid == TR::kKPerStage ? kAtomsPerStage : kvalid / 128;
+        const int nmma = kvalid == TR::kKPerStage ? kMmaPerStage : kvalid / TR::kMmaK;
+        if (elect_one()) {
 #pragma unroll
           for (int ka = 0; ka < kAtomsPerStage; ++ka) {
             if (ka < katoms) {
@@ -325,23 +326,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             }
           }
           tc_commit(empty_bar(slot));
-          issued = true;
-          if (++slot == kStages) {
-            slot = 0;
-            phase ^= 1u;
-          }
         }
-        if (!ok) break;
-        tc_commit(tmem_full_bar);
-        acc_phase ^= 1u;
+        __syncwarp();
+        issued = true;
+        if (++slot == kStages) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
-      // Make sure no MMA or TMEM copy of this CTA is still running before TMEM is freed.
-      if (issued) {
-        tc_commit(drain_bar);
-        lane_wait(drain_bar, 0, sync, 100000000ull, true);
-      }
+      if (!ok) break;
+      if (elect_one()) tc_commit(tmem_full_bar);
+      __syncwarp();
+      acc_phase ^= 1u;
     }
-    __syncwarp();
+    // Make sure no MMA or TMEM copy of this CTA is still running before TMEM is freed.
+    if (issued) {
+      if (elect_one()) tc_commit(drain_bar);
+      __syncwarp();
+      warp_wait(drain_bar, 0, sync, 100000000ull, true);
+    }
   } else {
     // ------------------------------------------------------------------ epilogue
     const int quad = warp & 3;         // TMEM lane quadrant this warp may read
