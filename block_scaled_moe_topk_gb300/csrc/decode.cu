@@ -555,7 +555,9 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
     // active expert a goes to row act_off[a] + (number of tokens below t routed to a).
     scatter_pairs(lane);
     named_barrier(1, 32 + 32 * kDEpiWarps);
-    if (lane == 0) {
+    // converged loop, one elected lane issues the copies; lane 0 alone polls the global
+    // counters and passes the verdict on (a warp barrier orders its acquire before the copies)
+    {
       int slot = 0;
       uint32_t phase = 0;
       int armed[kStages];
@@ -568,12 +570,16 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
         const int64_t row0 = (int64_t)kRowTile * act_mtb[a];
         const int K = P.K;
         for (int ks = ks0; ks < ks1; ++ks) {
-          if (!lane_wait(empty_bar(slot), phase ^ 1u, sync, p.timeout_ns)) {
+          if (!warp_wait(empty_bar(slot), phase ^ 1u, sync, p.timeout_ns)) {
             ok = false;
             break;
           }
           if (gi == 0 && !quant_seen) {
-            if (!wait_counter(p.sync + kSyncQuant, (uint32_t)T, p.sync, sync, p.timeout_ns)) {
+            bool seen = true;
+            if (lane == 0) seen = wait_counter(p.sync + kSyncQuant, (uint32_t)T, p.sync, sync, p.timeout_ns);
+            seen = __shfl_sync(0xffffffffu, seen, 0);
+            __syncwarp();
+            if (!seen) {
               ok = false;
               break;
             }
@@ -582,7 +588,11 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
           }
           if (gi == 1 && ready_a != a) {
             const uint32_t need = (uint32_t)(phs[0].NT * 2 * quads_of(a));
-            if (!wait_counter(p.sync + kSyncReady + a, need, p.sync, sync, p.timeout_ns)) {
+            bool ready = true;
+            if (lane == 0) ready = wait_counter(p.sync + kSyncReady + a, need, p.sync, sync, p.timeout_ns);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            __syncwarp();
+            if (!ready) {
               ok = false;
               break;
             }
@@ -591,11 +601,14 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
           }
           const int katoms = min(KPS, K - ks * KPS) / 128;
           const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
-          mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(G::kABytes + katoms * 512));
-          tma_load_2d(st, gi == 0 ? &p.tmap_x : &p.tmap_a2, full_bar(slot), ks * 128, (int)row0);
-          bulk_load(st + kSfaOff,
-                    (gi == 0 ? p.xs : p.a2s) + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
-                    (uint32_t)katoms * 512u, full_bar(slot));
+          if (elect_one()) {
+            mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(G::kABytes + katoms * 512));
+            tma_load_2d(st, gi == 0 ? &p.tmap_x : &p.tmap_a2, full_bar(slot), ks * 128, (int)row0);
+            bulk_load(st + kSfaOff,
+                      (gi == 0 ? p.xs : p.a2s) + ((row0 / 128) * (K / 128) + (int64_t)ks * kAtomsPerStage) * 512,
+                      (uint32_t)katoms * 512u, full_bar(slot));
+          }
+          __syncwarp();
           armed[slot] = (int)phase;
           if (++slot == kStages) {
             slot = 0;
@@ -604,7 +617,7 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
         }
       })
       for (int s = 0; s < kStages; ++s)
-        if (armed[s] >= 0) lane_wait(full_bar(s), (uint32_t)armed[s], sync, 100000000ull, true);
+        if (armed[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed[s], sync, 100000000ull, true);
     }
     __syncwarp();
   } else if (warp == kDWeightWarp) {
@@ -642,7 +655,7 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
         }
         const int katoms = min(KPS, K - ks * KPS) / 128;
         const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
-        if (lane == 0) {
+        if (elect_one()) {
           if (p.w_sf_tiled) {
             const int halves = n_rows > 128 ? 2 : 1;
             mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(TR::kBTxBytes + halves * katoms * 512));
@@ -678,9 +691,8 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
       }
     })
     cp_async_wait_all();
-    if (lane == 0)
-      for (int s = 0; s < kStages; ++s)
-        if (armed[s] >= 0) lane_wait(full_bar(s), (uint32_t)armed[s], sync, 100000000ull, true);
+    for (int s = 0; s < kStages; ++s)
+      if (armed[s] >= 0) warp_wait(full_bar(s), (uint32_t)armed[s], sync, 100000000ull, true);
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer: the warp runs the

@@ -212,7 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         }
         const int katoms = min(TR::kKPerStage, K - ks * TR::kKPerStage) / 128;
         const uint32_t st = sbase + (uint32_t)slot * kStageBytes;
-        if (lane == 0) {
+        // one elected lane of the converged warp issues the copies (as for the MMAs, this keeps
+        // their operands in uniform registers and the loop short)
+        if (elect_one()) {
           if (tma_warp) {
             // activation side, plus the weight codes when the scale warp is busy gathering
             mbar_arrive_expect_tx(full_bar(slot),
