@@ -15,11 +15,12 @@ import torch
 
 __all__ = [
     "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "MOE_SCHEDULE_AUTO", "MOE_SCHEDULE_CHAIN", "MOE_SCHEDULE_FUSED",
-    "MOE_SCHEDULE_CHAIN_BF16_H", "lib", "moe_status_string", "moe_workspace_bytes",
+    "MOE_SCHEDULE_CHAIN_BF16_H", "MOE_SCHEDULE_CHAIN_SINGLE_CTA", "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
     "moe_quantize_mx", "moe_a8w4_forward",
     "moe_a4w4_forward", "moe_forward_ex", "moe_a8w4_forward_prequant", "moe_a4w4_forward_prequant", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
-    "moe_read_device_status", "moe_forward_launch_count", "moe_forward_launch_count_ex", "moe_profile_forward",
+    "moe_read_device_status", "moe_forward_launch_count", "moe_forward_launch_count_ex", "moe_forward_launch_count_cfg",
+    "moe_forward_split_gemms", "moe_profile_forward",
     "workspace_views",
 ]
 
@@ -29,6 +30,7 @@ MOE_SCHEDULE_AUTO = 0   # the library's choice for the shape and T
 MOE_SCHEDULE_CHAIN = 1  # kernel chain, one CTA per 128 x 256 GEMM tile over the whole K
 MOE_SCHEDULE_FUSED = 2  # T <= 64: the whole layer in one persistent kernel
 MOE_SCHEDULE_CHAIN_BF16_H = 3  # kernel chain, GEMM1 writes bf16 h, a separate kernel requantises
+MOE_SCHEDULE_CHAIN_SINGLE_CTA = 4  # kernel chain with single-CTA GEMM tiles only (no pair split)
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_topk.so")
 
 STATUS_NAMES = {
@@ -95,6 +97,10 @@ def lib():
     L.moe_forward_launch_count.argtypes = [i64, i32, i32]
     L.moe_forward_launch_count_ex.restype = i32
     L.moe_forward_launch_count_ex.argtypes = [i64, i32, i32, i32]
+    L.moe_forward_launch_count_cfg.restype = i32
+    L.moe_forward_launch_count_cfg.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32]
+    L.moe_forward_split_gemms.restype = i32
+    L.moe_forward_split_gemms.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32]
     L.moe_profile_forward.restype = i32
     L.moe_profile_forward.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, P, sz, P, i32, i32,
                                       ctypes.POINTER(ctypes.c_float)]
@@ -148,6 +154,16 @@ def moe_forward_launch_count(T, H, I) -> int:
 
 def moe_forward_launch_count_ex(T, H, I, schedule) -> int:
     return int(lib().moe_forward_launch_count_ex(int(T), int(H), int(I), int(schedule)))
+
+
+def moe_forward_launch_count_cfg(T, H, I, E, k, fmt, schedule, prepacked_scales) -> int:
+    return int(lib().moe_forward_launch_count_cfg(int(T), int(H), int(I), int(E), int(k), int(fmt), int(schedule),
+                                                  int(bool(prepacked_scales))))
+
+
+def moe_forward_split_gemms(T, H, I, E, k, fmt, schedule, prepacked_scales) -> int:
+    return int(lib().moe_forward_split_gemms(int(T), int(H), int(I), int(E), int(k), int(fmt), int(schedule),
+                                             int(bool(prepacked_scales))))
 
 
 def moe_topk_route(gate_logits, k, topk_ids, topk_w, stream=None):
@@ -269,18 +285,25 @@ def moe_profile_forward(fmt, x, gate_logits, w1, w1_scale, w2, w2_scale, out, E,
     """One forward with a CUDA event between kernels; returns {kernel name: microseconds}."""
     T, H = x.shape
     I = w2.shape[-1] * 2
-    n = moe_forward_launch_count_ex(T, H, I, schedule)
+    n = moe_forward_launch_count_cfg(T, H, I, E, k, fmt, schedule, prepacked_scales)
+    split = moe_forward_split_gemms(T, H, I, E, k, fmt, schedule, prepacked_scales)
     us = (ctypes.c_float * max(n, 1))()
     _check(lib().moe_profile_forward(int(fmt), _p(x), _p(gate_logits), _p(w1), _p(w1_scale), _p(w2), _p(w2_scale),
                                      _p(out), T, H, I, int(E), int(k), _p(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream),
                                      int(bool(prepacked_scales)), int(schedule), us),
            "moe_profile_forward")
+    n_base = n - bin(max(split, 0)).count("1")
     if schedule == MOE_SCHEDULE_CHAIN_BF16_H:
-        names = KERNEL_NAMES_BF16_H if n == len(KERNEL_NAMES_BF16_H) else KERNEL_NAMES_BF16_H_SMALL
+        names = KERNEL_NAMES_BF16_H if n_base == len(KERNEL_NAMES_BF16_H) else KERNEL_NAMES_BF16_H_SMALL
     else:
         names = {len(KERNEL_NAMES): KERNEL_NAMES, len(KERNEL_NAMES_SMALL): KERNEL_NAMES_SMALL,
-                 1: KERNEL_NAMES_FUSED}[n]
+                 1: KERNEL_NAMES_FUSED}[n_base]
+    # a split GEMM: its pair kernel, then its tail pass
+    expand = {"gemm1": ("gemm1_pairs", "gemm1_tails") if split & 1 else ("gemm1",),
+              "gemm2": ("gemm2_pairs", "gemm2_tails") if split & 2 else ("gemm2",)}
+    names = [m for nm in names for m in expand.get(nm, (nm,))]
+    assert len(names) == n
     return {names[i]: float(us[i]) for i in range(n)}
 
 

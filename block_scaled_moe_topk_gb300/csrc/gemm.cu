@@ -67,9 +67,11 @@ struct Geo {
   static constexpr int kStages = AROWS == kRowTile ? 4 : (AROWS == 16 && ACT == 0 ? 6 : 5);
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kTileBaseOff = kBarOff + 256;      // M-tile prefix over experts, int32 [E+1]
-  // 64-row units: their own prefix over experts, int32 [E+1] (else the M-tile prefix serves)
+  // 64-row units, and the tail pass of A8W4 128-row tiles: their own prefix over experts,
+  // int32 [E+1] (else the M-tile prefix serves)
+  static constexpr bool kUnitTable = kUnitRows == 64 || (AROWS == kRowTile && ACT == 0);
   static constexpr int kUnitBaseOff = kTileBaseOff + 4 * (kMaxExperts + 1);
-  static constexpr int kTablesEnd = kUnitBaseOff + (kUnitRows == 64 ? 4 * (kMaxExperts + 1) : 0);
+  static constexpr int kTablesEnd = kUnitBaseOff + (kUnitTable ? 4 * (kMaxExperts + 1) : 0);
   static constexpr bool kOutStaging = AROWS == kRowTile;  // GEMM2 rows leave as TMA stores
   static constexpr int kOutStageOff = (kTablesEnd + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes =
@@ -98,6 +100,7 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   int E, N, K;
   int w_sf_tiled;
   int test_stall;
+  int tail_only;  // only the odd last M tile of each expert (the pair kernel took the rest)
 };
 
 template <int ACT, int EPI, int AROWS>
@@ -124,19 +127,23 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + G::kBarOff + 8 * (2 * kStages + 3));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int32_t* tile_base = reinterpret_cast<int32_t*>(smem + G::kTileBaseOff);
-  // work units per expert: its M tiles, or (64-row units) ceil(count / 64)
-  int32_t* unit_base = G::kUnitRows == 64 ? reinterpret_cast<int32_t*>(smem + G::kUnitBaseOff) : tile_base;
+  // work units per expert: its M tiles, (64-row units) ceil(count / 64), or (tail pass) its odd
+  // last M tile
+  const bool unit_table = G::kUnitRows == 64 || (G::kUnitTable && p.tail_only);
+  int32_t* unit_base = unit_table ? reinterpret_cast<int32_t*>(smem + G::kUnitBaseOff) : tile_base;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // the per-tile expert lookup (a binary search) reads shared memory, not global memory: it
   // sits on the producer's path at every tile boundary
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) tile_base[e] = p.mtile_base[e];
-  if (G::kUnitRows == 64 && threadIdx.x / 32 == 2) {  // exclusive prefix of ceil(count / 64), warp 2
+  if (unit_table && threadIdx.x / 32 == 2) {  // exclusive prefix of the units per expert, warp 2
     const int ln = threadIdx.x % 32;
     int running = 0;
     for (int e0 = 0; e0 < p.E; e0 += 32) {
       const int e = e0 + ln;
-      const int v = e < p.E ? (p.counts[e] + 63) / 64 : 0;
+      const int v = e >= p.E ? 0
+                    : G::kUnitRows == 64 ? (p.counts[e] + 63) / 64
+                                         : ((p.mtile_base[e + 1] - p.mtile_base[e]) & 1);
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -192,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
     bool ok = !p.test_stall;  // the test hook leaves every stage unfilled
     for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      const Tile tc = decode_tile(tile, unit_base, p.E, NT);  // tc.mt: unit index inside the expert
+      Tile tc = decode_tile(tile, unit_base, p.E, NT);  // tc.mt: unit index inside the expert
+      if (G::kUnitTable && p.tail_only) tc.mt = tile_base[tc.e + 1] - tile_base[tc.e] - 1;  // the last M tile
       const int64_t row0 = (int64_t)tile_base[tc.e] * kRowTile + (int64_t)tc.mt * G::kUnitRows;
       const int n0 = tc.nt * kNTile;
       const uint8_t* wsf_rows = p.w_sf + ((int64_t)tc.e * p.N + n0) * (K / 32);
@@ -353,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     const int half = (warp - 2) >> 2;  // accumulator columns [half*128, half*128 + 128)
     uint32_t acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile tc = decode_tile(tile, unit_base, p.E, NT);
+      Tile tc = decode_tile(tile, unit_base, p.E, NT);
+      if (G::kUnitTable && p.tail_only) tc.mt = tile_base[tc.e + 1] - tile_base[tc.e] - 1;
       const int row_local = tc.mt * G::kUnitRows + quad * 32 + lane;
       // a 64-row unit fills accumulator lanes 0..63 only: the warps of quadrants 2 and 3 keep
       // step with the tile hand-off (wait, release) and store nothing; so do the warps of
@@ -463,6 +472,7 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   p.w_sf = a.w_sf;
   p.w_sf_tiled = a.w_sf_tiled;
   p.test_stall = a.test_stall;
+  p.tail_only = a.tail_only;
   p.counts = a.counts;
   p.mtile_base = a.mtile_base;
   p.out_codes = a.out_codes;

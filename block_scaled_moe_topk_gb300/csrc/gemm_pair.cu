@@ -1,0 +1,488 @@
+// gemm_pair.cu -- the grouped block-scaled GEMMs of the expert layer on CTA pairs, for the
+// experts' whole pairs of M tiles (A8W4 or A4W4, weight scales in the 128x4 tile layout).
+//
+// Same contract as gemm.cu (GEMM1: SwiGLU + MX requant epilogue over the gate/up-interleaved
+// W1 rows, "feat(moe): FlyDSL MegaMoE fused EP-MoE integration", description: INTERLEAVE(g1u1);
+// GEMM2: bf16 rows).  An expert with m M tiles has m / 2 (rounded down) pair tiles here; its
+// odd last M tile, if any, is left to gemm.cu's tail pass (GemmArgs::tail_only), which runs
+// right after this kernel on the same stream.
+//
+// A pair tile is 256 routed rows -- two consecutive 128-row M tiles of one expert -- by 256
+// output columns, computed by a cluster of two CTAs on two SMs with tcgen05.mma.cta_group::2
+// (M = 256):
+//   * each CTA loads its own 128 activation rows and 128 of the 256 weight rows of the tile,
+//     so a CTA's shared-memory stage is 35 KiB instead of 50 KiB: the ring is 6 deep, which
+//     covers the load latency better than the single kernel's 4 stages;
+//   * each CTA stages the scales of all 256 weight rows of the tile (the MMA of each SM reads
+//     the weight scales of every output column from its own TMEM);
+//   * one elected lane of the even CTA's converged MMA warp issues the scale copies to TMEM and
+//     the MMAs for both; each CTA's TMEM receives the accumulator of its own 128 rows;
+//   * every TMA load of either CTA completes on the even CTA's "full" barrier, whose expected
+//     byte count the even CTA's producers post for both CTAs (local arrivals only: a remote
+//     arrive with release semantics stalls the issuing thread on a cluster-wide fence); the MMA
+//     commit releases the slot in both CTAs (multicast), and the accumulator hand-off goes to
+//     both epilogues, whose "TMEM free" arrivals go back to the even CTA.
+// Measured (V4-Pro A8W4, T = 8192): a pair stage costs ~0.32 us per SM against ~0.42 for the
+// single kernel's, so the pairs plus the tail pass run GEMM1 in 1.94 ms against 2.13 ms for
+// single-CTA tiles throughout.
+// Warp roles per CTA: 0 activation-side TMA, 10 weight-side TMA (both converged, copies issued
+// by an elected lane), 1 TMEM (+ MMA issue in the even CTA), 2..9 epilogue (as in gemm.cu).
+// Every wait is bounded; on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT, lets its copies and
+// MMAs drain, and both CTAs meet at the final cluster barrier before the pair's TMEM is freed.
+#include <cuda.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "gemm_common.cuh"
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPStages = 6;
+constexpr int kPThreads = 352;
+constexpr int kPEpiWarps = 8;
+constexpr int kPBWarp = 10;
+constexpr int kPHalfRows = 128;                    // weight rows per CTA (half of kNTile)
+constexpr int kPABytes = kRowTile * 128;           // 128 activation rows x 128 bytes
+constexpr int kPBBytes = kPHalfRows * 128;         // 128 weight rows x 128 bytes (smem footprint)
+constexpr int kPSfaOff = kPABytes + kPBBytes;
+constexpr int kPSfbOff = kPSfaOff + 1024;
+constexpr int kPStageBytes = kPSfbOff + 2048;      // 35 KiB, a multiple of 1024
+constexpr int kPBarOff = kPStages * kPStageBytes;
+constexpr int kPBaseOff = kPBarOff + 256;          // pair-tile prefix over experts, int32 [E+1]
+constexpr int kPTileBaseOff = kPBaseOff + 4 * (kMaxExperts + 1);  // M-tile prefix, int32 [E+1]
+constexpr int kPSmemBytes = kPTileBaseOff + 4 * (kMaxExperts + 1) + 1024;
+constexpr uint32_t kPTmemCols = 512;
+constexpr uint32_t kPSfCol0 = 256;
+constexpr uint32_t kPSfSlotCols = 32;
+static_assert(kPSmemBytes <= 232448, "pair GEMM shared memory");
+static_assert(kPStages * kPSfSlotCols <= kPTmemCols - kPSfCol0, "pair GEMM TMEM scale slots");
+
+struct PairParams {  // 64-byte aligned through its CUtensorMap members
+  CUtensorMap tmap_act;  // activation codes [rows_cap, K or K/2], box 128 B x 128 rows
+  CUtensorMap tmap_w;    // weights [E, N, K/2], box 128 K x 128 rows x 1
+  CUtensorMap tmap_asf;  // activation scales as rows of 256 bytes, box 256 x (2 * atoms per stage)
+  CUtensorMap tmap_wsf;  // prepacked weight scales as rows of 256 bytes, same box
+  const int32_t* counts;
+  const int32_t* mtile_base;  // expert e's rows start at row 128 * mtile_base[e]
+  uint8_t* out_codes;
+  uint8_t* out_sf;
+  uint16_t* out_bf16;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int E, N, K;
+  int test_stall;
+};
+
+struct PairTile {
+  int e, pm, nt;
+};
+
+// Pair tiles of expert e occupy [base[e]*NT, base[e+1]*NT), pair index fastest.
+__device__ __forceinline__ PairTile decode_pair_tile(int64_t tile, const int32_t* base, int E, int NT) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)base[mid] * NT <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  const int pe = base[lo + 1] - base[lo];
+  const int64_t local = tile - (int64_t)base[lo] * NT;
+  PairTile t;
+  t.e = lo;
+  t.nt = (int)(local / pe);
+  t.pm = (int)(local % pe);
+  return t;
+}
+
+// Spin for about `cycles` SM clock cycles (used on the abort path only, to let copies that
+// were issued but can no longer be waited for land before the CTA leaves).
+__device__ __noinline__ void grace_spin(uint64_t cycles) {
+  const uint64_t t0 = clock64();
+  while (clock64() - t0 < cycles) {
+  }
+}
+
+template <int ACT, int EPI>
+__global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __grid_constant__ PairParams p) {
+  using TR = ActTraits<ACT>;
+  constexpr int kMmaPerStage = TR::kKPerStage / TR::kMmaK;  // 4
+  constexpr int kAtomsPerStage = TR::kKPerStage / 128;      // k-atoms of 4 scale blocks
+  constexpr uint32_t kSfaCols = kAtomsPerStage * 4;
+  constexpr uint32_t kScaleBoxBytes = kAtomsPerStage * 512;
+  constexpr uint32_t kBHalfTx = TR::kBTxBytes / 2;          // global bytes of 128 weight rows
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kPBarOff;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kPStages + s); };
+  const uint32_t tmem_full_bar = bar0 + 8u * (2 * kPStages);
+  const uint32_t tmem_empty_bar = tmem_full_bar + 8;
+  const uint32_t drain_bar = tmem_full_bar + 16;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kPBarOff + 8 * (2 * kPStages + 3));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int32_t* pair_base = reinterpret_cast<int32_t*>(smem + kPBaseOff);
+  int32_t* tile_base = reinterpret_cast<int32_t*>(smem + kPTileBaseOff);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(full_bar(s), 2);    // expect_tx arrivals of warps 0 and 10 of the even CTA
+      mbar_init(empty_bar(s), 1);   // the pair's MMA commit
+    }
+    mbar_init(tmem_full_bar, 1);
+    mbar_init(tmem_empty_bar, 2 * kPEpiWarps);  // epilogue warps of both CTAs
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // Expert tile prefixes in shared memory (the per-tile lookups sit on the producers' path):
+  // M tiles as given, and pair tiles per expert, ceil(M tiles / 2), prefixed by warp 2.
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) tile_base[e] = p.mtile_base[e];
+  if (warp == 2) {
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? (p.mtile_base[e + 1] - p.mtile_base[e]) >> 1 : 0;  // whole pairs only
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) pair_base[e] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pair_base[E] = running;
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), kPTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers initialised in both CTAs before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const Sync sync{abort_flag, p.status, p.timeout_ns, bar0};
+  const int NT = p.N / kNTile;
+  const int K = p.K;
+  const int nks = (K + TR::kKPerStage - 1) / TR::kKPerStage;
+  const int64_t total_tiles = (int64_t)pair_base[E] * NT;
+  const int64_t first_tile = cluster_index();
+  const int64_t tile_step = cluster_count();
+  const uint32_t leader_full0 = mapa_shared(full_bar(0), 0);
+
+  if (warp == 0 || warp == kPBWarp) {
+    // ------------------------------------------------------------------ producers (converged)
+    const bool act_warp = warp == 0;
+    {
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = !p.test_stall;  // the test hook leaves every stage unfilled
+      for (int64_t tile = first_tile; ok && tile < total_tiles; tile += tile_step) {
+        const PairTile pt = decode_pair_tile(tile, pair_base, E, NT);
+        const int mt = 2 * pt.pm + (int)rank;
+        const int mt_e = tile_base[pt.e + 1] - tile_base[pt.e];
+        const bool real = mt < mt_e;
+        const bool peer_real = 2 * pt.pm + 1 < mt_e;  // the odd CTA has rows in this tile
+        const int64_t row0 = ((int64_t)tile_base[pt.e] + mt) * kRowTile;
+        const int n0 = pt.nt * kNTile;
+        const int asf_y0 = (int)(2 * ((row0 / 128) * (K / 128)));             // scale rows of 256 B
+        const int wsf_y0 = (int)(2 * ((((int64_t)pt.e * p.N + n0) / 128) * (K / 128)));
+        const int wsf_half = 2 * (K / 128);                                     // next 128 weight rows
+        // bytes both CTAs land on the even CTA's barrier per stage, posted by the even CTA (a
+        // load of the odd CTA may complete before the post, which the barrier's signed
+        // transaction count allows: the phase cannot complete before both posts arrived)
+        const uint32_t act_tx = ((uint32_t)kPABytes + kScaleBoxBytes) * (peer_real ? 2u : 1u);
+        const uint32_t w_tx = 2u * (kBHalfTx + 2u * kScaleBoxBytes);
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!warp_wait(empty_bar(slot), phase ^ 1u, sync, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + (uint32_t)slot * kPStageBytes;
+          const uint32_t lfull = leader_full0 + 8u * slot;
+          const int ky = 2 * ks * kAtomsPerStage;
+          if (elect_one()) {
+            if (act_warp) {
+              if (leader) mbar_arrive_expect_tx(full_bar(slot), act_tx);
+              if (real) {
+                tma_load_2d_pair(st, &p.tmap_act, lfull, ks * 128, (int)row0);
+                tma_load_2d_pair(st + kPSfaOff, &p.tmap_asf, lfull, 0, asf_y0 + ky);
+              }
+            } else {
+              if (leader) mbar_arrive_expect_tx(full_bar(slot), w_tx);
+              tma_load_3d_pair(st + kPABytes, &p.tmap_w, lfull, ks * 128, n0 + (int)rank * kPHalfRows, pt.e);
+              tma_load_2d_pair(st + kPSfbOff, &p.tmap_wsf, lfull, 0, wsf_y0 + ky);
+              tma_load_2d_pair(st + kPSfbOff + kScaleBoxBytes, &p.tmap_wsf, lfull, 0, wsf_y0 + wsf_half + ky);
+            }
+          }
+          __syncwarp();
+          if (++slot == kPStages) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    // The warp runs the loop converged and one elected lane issues each tcgen05.cp / mma /
+    // commit (see gemm.cu), with every descriptor and TMEM address precomputed.
+    if (leader) {
+      int slot = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      // descriptors of slot 0; a slot adds kPStageBytes, an MMA step 32 bytes (start address
+      // field, in 16-byte units; shared-memory offsets stay below 2^18, so no carry)
+      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(sbase + kPABytes, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t sfa_desc0 = smem_desc(sbase + kPSfaOff, 128, 128, kLayoutNone);
+      const uint64_t sfb_desc0 = smem_desc(sbase + kPSfbOff, 128, 128, kLayoutNone);
+      constexpr uint64_t kSlotStep = kPStageBytes >> 4;
+      constexpr uint32_t kSfbCols = 8;  // TMEM columns of the 256 weight rows' scales per k-atom
+      for (int64_t tile = first_tile; ok && tile < total_tiles; tile += tile_step) {
+        if (!warp_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!warp_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = (uint64_t)slot * kSlotStep;
+          const uint32_t sf_col = tmem_base + kPSfCol0 + (uint32_t)slot * kPSfSlotCols;
+          const int kvalid = min(TR::kKPerStage, K - ks * TR::kKPerStage);
+          const bool el = elect_one();
+          if (el && kvalid == TR::kKPerStage) {
+#pragma unroll
+            for (int ka = 0; ka < kAtomsPerStage; ++ka) {
+              tc_cp_pair_32x128b_warpx4(sf_col + ka * 4, sfa_desc0 + so + ka * 32);
+              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols, sfb_desc0 + so + ka * 32);
+              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols + 4,
+                                        sfb_desc0 + so + (kScaleBoxBytes >> 4) + ka * 32);
+            }
+#pragma unroll
+            for (int j = 0; j < kMmaPerStage; ++j) {
+              constexpr int kBlkPerMma = TR::kMmaK / 32;
+              const int kblk = j * kBlkPerMma;
+              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3), 2 * kRowTile);
+              const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
+              if (ACT == 0)
+                tc_mma_pair_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
+                                     sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
+              else
+                tc_mma_pair_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
+                                 sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
+            }
+          } else if (el) {
+            // the last stage of a K that is not a multiple of the stage depth (A4W4: one k-atom)
+            const int katoms = kvalid / 128;
+            const int nmma = kvalid / TR::kMmaK;
+            for (int ka = 0; ka < katoms; ++ka) {
+              tc_cp_pair_32x128b_warpx4(sf_col + ka * 4, sfa_desc0 + so + ka * 32);
+              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols, sfb_desc0 + so + ka * 32);
+              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols + 4,
+                                        sfb_desc0 + so + (kScaleBoxBytes >> 4) + ka * 32);
+            }
+            for (int j = 0; j < nmma; ++j) {
+              const int kblk = j * (TR::kMmaK / 32);
+              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3), 2 * kRowTile);
+              const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
+              if (ACT == 0)
+                tc_mma_pair_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
+                                     sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
+              else
+                tc_mma_pair_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
+                                 sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
+            }
+          }
+          if (el) tc_commit_pair_mc(empty_bar(slot), 0x3);
+          __syncwarp();
+          issued = true;
+          if (++slot == kPStages) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (elect_one()) tc_commit_pair_mc(tmem_full_bar, 0x3);
+        __syncwarp();
+        acc_phase ^= 1u;
+      }
+      if (issued) {
+        // no MMA or TMEM copy of the pair may still run when TMEM is freed
+        if (elect_one()) tc_commit_pair(drain_bar);
+        __syncwarp();
+        warp_wait(drain_bar, 0, sync, 100000000ull, true);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const uint32_t leader_tmem_empty = mapa_shared(tmem_empty_bar, 0);
+    uint32_t acc_phase = 0;
+    for (int64_t tile = first_tile; tile < total_tiles; tile += tile_step) {
+      const PairTile pt = decode_pair_tile(tile, pair_base, E, NT);
+      const int mt = 2 * pt.pm + (int)rank;
+      const int row_local = mt * kRowTile + quad * 32 + lane;
+      const bool valid = row_local < p.counts[pt.e];  // false for every row of a missing M tile
+      const int64_t prow = (int64_t)tile_base[pt.e] * kRowTile + row_local;
+      if (!warp_wait(tmem_full_bar, acc_phase, sync, p.timeout_ns)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
+      float acc[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(taddr + c * 32, acc + 32 * c);
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);  // registers hold the tile
+      acc_phase ^= 1u;
+      store_acc_rows<ACT, EPI>(acc, valid, prow, pt.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16);
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // both CTAs done with the pair's TMEM
+  // Without an abort every stage a producer filled was consumed by the pair's MMAs, so no copy
+  // is in flight.  After an abort in either CTA, loads that were issued but never waited for
+  // may still be landing in this CTA's shared memory or on the even CTA's barriers: give them
+  // time (they complete within microseconds) before either CTA can leave.
+  const uint32_t peer_abort = ld_shared_cluster_u32(mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u));
+  if (*abort_flag || peer_abort) grace_spin(2000000ull);
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kPTmemCols);
+}
+
+// ---------------------------------------------------------------------- host side
+// Scale arrays in the 128x4 tile layout viewed as rows of 256 bytes; a stage's k-atoms of one
+// 128-row block are 2 * atoms consecutive rows.
+CUresult encode_scale_rows(EncodeTiledFn encode, CUtensorMap* m, const uint8_t* base, uint64_t bytes, int atoms) {
+  const cuuint64_t dims[2] = {256, (cuuint64_t)(bytes / 256)};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {256, (cuuint32_t)(2 * atoms)};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int ACT, int EPI>
+cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
+  // per device, computed once; host threads racing here compute and store the same value
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters[dev].load(std::memory_order_acquire) == 0) {
+    err = cudaFuncSetAttribute(moe_gemm_pair_kernel<ACT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kPSmemBytes);
+    if (err != cudaSuccess) return err;
+    int n = 0;
+    cfg.gridDim = dim3(2 * a.num_sms / 2);
+    err = cudaOccupancyMaxActiveClusters(&n, moe_gemm_pair_kernel<ACT, EPI>, &cfg);
+    if (err != cudaSuccess) return err;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    max_clusters[dev].store(n, std::memory_order_release);
+  }
+  EncodeTiledFn encode = get_encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+
+  PairParams p;
+  memset(&p, 0, sizeof(p));
+  const int K = a.K;
+  const int atoms = ActTraits<ACT>::kKPerStage / 128;
+  const uint64_t act_row_bytes = ACT == 0 ? (uint64_t)K : (uint64_t)K / 2;
+  {
+    const cuuint64_t dims[2] = {act_row_bytes, (cuuint64_t)a.rows_cap};
+    const cuuint64_t strides[1] = {act_row_bytes};
+    const cuuint32_t box[2] = {128, (cuuint32_t)kRowTile};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&p.tmap_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.act), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t row_bytes = (uint64_t)K / 2;
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * (uint64_t)a.N};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kPHalfRows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r;
+    if (ACT == 0) {
+      const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)a.N, (cuuint64_t)a.E};
+      r = encode(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(a.w), dims, strides, box,
+                 es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      const cuuint64_t dims[3] = {row_bytes, (cuuint64_t)a.N, (cuuint64_t)a.E};
+      r = encode(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.w), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  const uint64_t asf_bytes = (uint64_t)(a.rows_cap / 128) * (uint64_t)(K / 128) * 512u;
+  const uint64_t wsf_bytes = (uint64_t)a.E * (uint64_t)(a.N / 128) * (uint64_t)(K / 128) * 512u;
+  if (encode_scale_rows(encode, &p.tmap_asf, a.act_sf, asf_bytes, atoms) != CUDA_SUCCESS ||
+      encode_scale_rows(encode, &p.tmap_wsf, a.w_sf, wsf_bytes, atoms) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  p.counts = a.counts;
+  p.mtile_base = a.mtile_base;
+  p.out_codes = a.out_codes;
+  p.out_sf = a.out_sf;
+  p.out_bf16 = a.out_bf16;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  p.E = a.E;
+  p.N = a.N;
+  p.K = a.K;
+  p.test_stall = a.test_stall;
+  // pair tiles <= M tiles / 2: a bound on the clusters that can find work
+  const int64_t clusters = std::min<int64_t>(std::min<int64_t>(max_clusters[dev].load(std::memory_order_acquire), a.num_sms / 2), a.max_tiles);
+  if (clusters <= 0) return cudaSuccess;
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<ACT, EPI>, p);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t s) {
+  if (!a.w_sf_tiled) return cudaErrorInvalidValue;  // pairs stage prepacked weight scales only
+  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_pair_typed<0, 0>(a, s) : launch_pair_typed<0, 1>(a, s);
+  return a.epilogue == 0 ? launch_pair_typed<1, 0>(a, s) : launch_pair_typed<1, 1>(a, s);
+}
+
+}  // namespace moe

@@ -140,10 +140,10 @@ int test_stall_producer() {
 // Kernel chain, T > 64: route, scan, scatter, quant, gemm1, gemm2, combine; T <= 64:
 // route_sort, quant, gemm1, gemm2, combine.  Fused schedule (T <= 64): one decode kernel.
 constexpr int kForwardKernels = 7;
-constexpr int kMaxForwardKernels = 8;  // the chain with the bf16-out GEMM1 and its requant kernel
+constexpr int kMaxForwardKernels = 9;  // the chain with both GEMMs split (pair kernel + tail pass)
 bool valid_schedule(int schedule) {
   return schedule == MOE_SCHEDULE_AUTO || schedule == MOE_SCHEDULE_CHAIN || schedule == MOE_SCHEDULE_FUSED ||
-         schedule == MOE_SCHEDULE_CHAIN_BF16_H;
+         schedule == MOE_SCHEDULE_CHAIN_BF16_H || schedule == MOE_SCHEDULE_CHAIN_SINGLE_CTA;
 }
 bool use_fused(int64_t T, int schedule, int H, int I) {
   return schedule == MOE_SCHEDULE_FUSED || (schedule == MOE_SCHEDULE_AUTO && moe::decode_auto(T, H, I));
@@ -153,6 +153,24 @@ int launch_count(int64_t T, int H, int I, int schedule = MOE_SCHEDULE_AUTO) {
   if (use_fused(T, schedule, H, I)) return 1;
   const int requant = schedule == MOE_SCHEDULE_CHAIN_BF16_H ? 1 : 0;  // the separate requant kernel
   return (T <= moe::kSmallRouteTokens ? 5 : kForwardKernels) + requant;
+}
+// Activation rows a single-CTA GEMM of reduction length K stages per K stage (GemmArgs::a_rows).
+int gemm_a_rows(int64_t T, int E, int k, int K) {
+  if (T <= 16) return 16;
+  const bool few_rows = T * (int64_t)k <= (int64_t)moe::kUnit64MaxRowsPerExpert * E;
+  return few_rows && K / 128 >= moe::kUnit64MinStages ? 64 : kRowTile;
+}
+// Whether the chain runs a GEMM of N output columns and reduction length K as the pair kernel
+// plus the tail pass (moe::gemm_pair_split).
+bool split_gemm(int64_t T, int E, int k, int afmt, bool prepacked, int schedule, int N, int K) {
+  if (schedule == MOE_SCHEDULE_CHAIN_SINGLE_CTA || schedule == MOE_SCHEDULE_CHAIN_BF16_H) return false;
+  return moe::gemm_pair_split(T, E, k, afmt, prepacked, N, gemm_a_rows(T, E, k, K));
+}
+int launch_count_cfg(int64_t T, int H, int I, int E, int k, int afmt, int schedule, bool prepacked) {
+  const int n = launch_count(T, H, I, schedule);
+  if (n <= 1) return n;
+  return n + (split_gemm(T, E, k, afmt, prepacked, schedule, 2 * I, H) ? 1 : 0) +
+         (split_gemm(T, E, k, afmt, prepacked, schedule, H, I) ? 1 : 0);
 }
 
 // x is bf16 [T, H] when x_scale is null, else prequantised codes [T, H or H/2] with canonical
@@ -293,12 +311,21 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   g1.test_stall = test_stall_producer();
   // T <= 16: no expert receives more than T rows (a token routes to an expert at most once);
   // few rows per expert on average and a long K: 64-row work units
-  const bool few_rows = T * (int64_t)k <= (int64_t)moe::kUnit64MaxRowsPerExpert * E;
-  auto a_rows_for = [&](int K) {
-    if (T <= 16) return 16;
-    return few_rows && K / 128 >= moe::kUnit64MinStages ? 64 : kRowTile;
-  };
+  auto a_rows_for = [&](int K) { return gemm_a_rows(T, E, k, K); };
   g1.a_rows = a_rows_for(H);
+  // a GEMM, split into the pair kernel and the tail pass where that pays (split_gemm)
+  auto run_gemm = [&](const moe::GemmArgs& g) -> cudaError_t {
+    if (g.epilogue != 2 && split_gemm(T, E, k, afmt, tiled_scales, schedule, g.N, g.K)) {
+      cudaError_t e = moe::launch_gemm_pair(g, s);
+      if (e != cudaSuccess) return e;
+      e = mark();
+      if (e != cudaSuccess) return e;
+      moe::GemmArgs t = g;
+      t.tail_only = 1;
+      return moe::launch_gemm(t, s);
+    }
+    return moe::launch_gemm(g, s);
+  };
   const bool bf16_h = schedule == MOE_SCHEDULE_CHAIN_BF16_H;
   if (bf16_h) {
     // GEMM1 leaves h = SwiGLU(acc) as bf16 rows in the y2 region; a separate kernel requantises
@@ -308,7 +335,7 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
     g1.out_sf = nullptr;
     g1.out_bf16 = reinterpret_cast<uint16_t*>(at(L.y2));
   }
-  MOE_CUDA_TRY(moe::launch_gemm(g1, s));
+  MOE_CUDA_TRY(run_gemm(g1));
   MOE_CUDA_TRY(mark());
   if (bf16_h) {
     moe::RequantArgs rq{reinterpret_cast<const uint16_t*>(at(L.y2)), inv_padded, T * (int64_t)k, I, afmt, at(L.a2),
@@ -330,7 +357,7 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   g2.out_codes = nullptr;
   g2.out_sf = nullptr;
   g2.out_bf16 = reinterpret_cast<uint16_t*>(at(L.y2));
-  MOE_CUDA_TRY(moe::launch_gemm(g2, s));
+  MOE_CUDA_TRY(run_gemm(g2));
   MOE_CUDA_TRY(mark());
 
   moe::CombineArgs ca{reinterpret_cast<const uint16_t*>(at(L.y2)), tw, inv_padded, T, H, k, static_cast<uint16_t*>(out)};
@@ -509,6 +536,20 @@ int moe_forward_launch_count_ex(int64_t T, int H, int I, int schedule) {
   return launch_count(T, H, I, schedule);
 }
 
+int moe_forward_launch_count_cfg(int64_t T, int H, int I, int E, int k, int fmt, int schedule,
+                                 int prepacked_scales) {
+  if (!valid_schedule(schedule) || (fmt != MOE_ACT_MXFP8 && fmt != MOE_ACT_MXFP4)) return -1;
+  return launch_count_cfg(T, H, I, E, k, fmt == MOE_ACT_MXFP8 ? 0 : 1, schedule, prepacked_scales != 0);
+}
+
+int moe_forward_split_gemms(int64_t T, int H, int I, int E, int k, int fmt, int schedule, int prepacked_scales) {
+  if (!valid_schedule(schedule) || (fmt != MOE_ACT_MXFP8 && fmt != MOE_ACT_MXFP4)) return -1;
+  if (launch_count(T, H, I, schedule) <= 1) return 0;
+  const int afmt = fmt == MOE_ACT_MXFP8 ? 0 : 1;
+  const bool pp = prepacked_scales != 0;
+  return (split_gemm(T, E, k, afmt, pp, schedule, 2 * I, H) ? 1 : 0) | (split_gemm(T, E, k, afmt, pp, schedule, H, I) ? 2 : 0);
+}
+
 moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* logits, const uint8_t* w1,
                                  const uint8_t* w1s, const uint8_t* w2, const uint8_t* w2s, void* out, int64_t T,
                                  int H, int I, int E, int k, void* ws, size_t ws_bytes, void* stream,
@@ -522,7 +563,7 @@ moe_status_t moe_profile_forward(moe_act_fmt_t fmt, const void* x, const float* 
   if (st == MOE_OK)
     st = forward(x, nullptr, logits, w1, w1s, w2, w2s, out, T, H, I, E, k, ws, ws_bytes, stream, fmt,
                  prepacked_scales != 0, ev, schedule);
-  const int nk = launch_count(T, H, I, schedule);
+  const int nk = launch_count_cfg(T, H, I, E, k, fmt == MOE_ACT_MXFP8 ? 0 : 1, schedule, prepacked_scales != 0);
   if (st == MOE_OK && T > 0) {
     if (cudaEventSynchronize(ev[nk]) != cudaSuccess) st = MOE_ERR_CUDA;
     for (int i = 0; i < nk && st == MOE_OK; ++i) {

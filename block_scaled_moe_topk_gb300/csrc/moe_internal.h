@@ -128,6 +128,8 @@ struct GemmArgs {
   int test_stall;         // test hook: the producer issues nothing, so the MMA warp's wait expires
   int a_rows;             // single-CTA tiles: activation rows staged per K stage (16, 64 or 128;
                           // 16 requires every tile to hold at most 16 routed rows)
+  int tail_only;          // single-CTA tiles, A8W4, 128 rows: only each expert's odd last M tile
+                          // (after launch_gemm_pair took the whole pairs)
 };
 // Single-CTA GEMMs stage 16 activation rows when T <= 16, and 64 rows (in 64-row work units)
 // when the batch routes at most this many rows per expert on average (T * k <= 16 * E) and the
@@ -137,6 +139,19 @@ constexpr int kUnit64MaxRowsPerExpert = 16;
 constexpr int kUnit64MinStages = 16;
 // gemm.cu: one CTA per 128-row x 256-column tile (any weight-scale layout).
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+// gemm_pair.cu: the whole pairs of each expert's M tiles on CTA pairs (prepacked weight scales,
+// N a multiple of 256); gemm.cu's tail pass (tail_only) then takes each odd last M tile.
+cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t s);
+// The kernel chain splits a GEMM into the pair kernel and the tail pass when its tiles are the
+// 128-row A8W4 ones, the weight scales are prepacked, N is a multiple of 256, and the batch
+// routes at least kPairMinRowsPerExpert rows per expert on average (then about half the
+// experts or more have a second M tile): measured on V4-Pro A8W4, GEMM1 -8.7 % and GEMM2 -6.8 %
+// at T = 8192, -4.7 % / -3 % at T = 16384, equal at T = 32768.
+constexpr int kPairMinRowsPerExpert = 128;
+inline bool gemm_pair_split(int64_t T, int E, int k, int act_fmt, bool prepacked, int N, int a_rows) {
+  return act_fmt == 0 && prepacked && N % kNTile == 0 && a_rows == kRowTile &&
+         T * (int64_t)k >= (int64_t)kPairMinRowsPerExpert * E;
+}
 
 
 // decode.cu: the whole layer for a small batch in one persistent kernel (T <= kDecodeMaxTokens).

@@ -88,7 +88,13 @@ typedef enum {
  * How a forward call schedules its work (moe_forward_ex, moe_profile_forward).
  *   MOE_SCHEDULE_CHAIN  the kernel chain: routing + sort, quantiser, GEMM1, GEMM2, combine;
  *                       each GEMM runs one CTA per 128-row x 256-column tile over the whole K;
- *                       GEMM2 rows are stored as bf16 before the combine.
+ *                       GEMM2 rows are stored as bf16 before the combine.  With A8W4,
+ *                       prepacked weight scales, 128-row tiles, an N (2I for GEMM1, H for GEMM2)
+ *                       that is a multiple of 256 and T * k >= 128 * E, a GEMM runs as two
+ *                       kernels: the experts' whole pairs of M tiles on CTA pairs
+ *                       (cta_group::2), then each expert's odd last M tile on single CTAs
+ *                       (bit-identical to CHAIN_SINGLE_CTA, faster at large T).
+ *   MOE_SCHEDULE_CHAIN_SINGLE_CTA  the kernel chain with single-CTA GEMM tiles throughout.
  *   MOE_SCHEDULE_FUSED  T <= 64 and H <= 16384 only (else MOE_ERR_UNSUPPORTED_SHAPE): the whole layer in one
  *                       persistent kernel on every SM ("feat(moe): FlyDSL MegaMoE fused EP-MoE
  *                       integration", description: one fused step for dispatch + gemm1 + quant
@@ -117,7 +123,8 @@ typedef enum {
   MOE_SCHEDULE_AUTO = 0,
   MOE_SCHEDULE_CHAIN = 1,
   MOE_SCHEDULE_FUSED = 2,
-  MOE_SCHEDULE_CHAIN_BF16_H = 3
+  MOE_SCHEDULE_CHAIN_BF16_H = 3,
+  MOE_SCHEDULE_CHAIN_SINGLE_CTA = 4
 } moe_schedule_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -351,12 +358,23 @@ moe_status_t moe_forward_ex(const moe_forward_args_t* args);
 moe_status_t moe_read_device_status(const void* workspace, void* stream, moe_status_t* status_out);
 
 /* Number of kernels one forward call of T tokens, hidden size H and intermediate size I
- * launches under MOE_SCHEDULE_AUTO: 0 for T = 0, 1 when the fused kernel is chosen, else the
- * kernel chain's 5 (T <= 64: routing and sort in one kernel) or 7. */
+ * launches under MOE_SCHEDULE_AUTO with canonical weight scales: 0 for T = 0, 1 when the fused
+ * kernel is chosen, else the kernel chain's 5 (T <= 64: routing and sort in one kernel) or 7. */
 int moe_forward_launch_count(int64_t T, int H, int I);
 
-/* The same for a given schedule (moe_schedule_t); -1 for an unknown schedule. */
+/* The same for a given schedule (moe_schedule_t), canonical weight scales; -1 for an unknown
+ * schedule. */
 int moe_forward_launch_count_ex(int64_t T, int H, int I, int schedule);
+
+/* The exact count for any forward: E experts, top-k, activation format `fmt`, the schedule, and
+ * whether the weight scales are prepacked (a GEMM split into its pair kernel and tail pass
+ * counts as two launches, see MOE_SCHEDULE_CHAIN); -1 for an unknown schedule or format. */
+int moe_forward_launch_count_cfg(int64_t T, int H, int I, int E, int k, int fmt, int schedule,
+                                 int prepacked_scales);
+
+/* Which GEMMs of that forward run split into their pair kernel and tail pass: bit 0 GEMM1,
+ * bit 1 GEMM2 (0 for the fused schedule); -1 for an unknown schedule or format. */
+int moe_forward_split_gemms(int64_t T, int H, int I, int E, int k, int fmt, int schedule, int prepacked_scales);
 
 /*
  * Profiling form of the forward: enqueues exactly the launch sequence of
@@ -365,10 +383,11 @@ int moe_forward_launch_count_ex(int64_t T, int H, int I, int schedule);
  * schedule `schedule` (moe_schedule_t, as in moe_forward_ex),
  * with a CUDA event recorded before the first kernel and after each kernel,
  * waits for the last event, and writes the duration of each kernel in
- * microseconds to kernel_us[moe_forward_launch_count_ex(T, schedule)] (HOST array),
- * in launch order: route, scan, scatter, quant, gemm1, gemm2, combine (chain, T > 64),
- * route_sort, quant, gemm1, gemm2, combine (chain, T <= 64) or decode (fused); the bf16-out
- * chain adds requant after gemm1.
+ * microseconds to kernel_us[moe_forward_launch_count_cfg(T, H, I, E, k, fmt, schedule,
+ * prepacked_scales)] (HOST array), in launch order: route, scan, scatter, quant, gemm1, gemm2,
+ * combine (chain, T > 64), route_sort, quant, gemm1, gemm2, combine (chain, T <= 64) or decode
+ * (fused); the bf16-out chain adds requant after gemm1, and a split GEMM contributes two
+ * entries (its pair kernel, then its tail pass).
  * Arguments and errors as for the forward; additionally synchronises on its
  * own events (so it is not graph-capturable) and creates/destroys them.
  */

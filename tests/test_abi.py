@@ -118,6 +118,28 @@ def test_forward_launch_count():
     assert moe.moe_forward_launch_count_ex(3, *flash, 9) == -1
     assert moe.moe_forward_launch_count_ex(3, *flash, moe.MOE_SCHEDULE_CHAIN_BF16_H) == 6
     assert moe.moe_forward_launch_count_ex(100, *pro, moe.MOE_SCHEDULE_CHAIN_BF16_H) == 8
+    assert moe.moe_forward_launch_count_ex(65, *pro, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA) == 7
+
+
+def test_forward_launch_count_with_split_gemms():
+    """The exact count: a GEMM split into its pair kernel and tail pass (A8W4, prepacked scales,
+    128-row tiles, N % 256 == 0, T * k >= 128 * E) counts twice."""
+    pro, a8, a4 = (7168, 3072), moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4
+    auto, chain = moe.MOE_SCHEDULE_AUTO, moe.MOE_SCHEDULE_CHAIN
+    cfg, split = moe.moe_forward_launch_count_cfg, moe.moe_forward_split_gemms
+    assert (cfg(8192, *pro, 384, 6, a8, auto, True), split(8192, *pro, 384, 6, a8, auto, True)) == (9, 3)
+    assert (cfg(8192, *pro, 384, 6, a8, chain, True), split(8192, *pro, 384, 6, a8, chain, True)) == (9, 3)
+    assert (cfg(8191, *pro, 384, 6, a8, auto, True), split(8191, *pro, 384, 6, a8, auto, True)) == (7, 0)  # < 128 rows / expert
+    assert cfg(8192, *pro, 384, 6, a8, auto, False) == 7                     # canonical weight scales
+    assert cfg(8192, *pro, 384, 6, a4, auto, True) == 7                      # A4W4
+    assert cfg(8192, *pro, 384, 6, a8, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA, True) == 7
+    assert cfg(8192, *pro, 384, 6, a8, moe.MOE_SCHEDULE_CHAIN_BF16_H, True) == 8
+    assert (cfg(1, *pro, 384, 6, a8, auto, True), split(1, *pro, 384, 6, a8, auto, True)) == (1, 0)  # fused
+    assert (cfg(0, *pro, 384, 6, a8, auto, True), split(0, *pro, 384, 6, a8, auto, True)) == (0, 0)
+    # GEMM2 of H = 384 has a 128-column last N tile: only GEMM1 (N = 2I = 256) splits
+    assert (cfg(512, 384, 128, 8, 2, a8, auto, True), split(512, 384, 128, 8, 2, a8, auto, True)) == (8, 1)
+    assert split(512, 256, 128, 8, 2, a8, auto, True) == 3
+    assert cfg(512, 256, 128, 8, 2, a8, 9, True) == -1 and split(512, 256, 128, 8, 2, 5, auto, True) == -1
 
 
 def test_forward_ex_schedule_validation():

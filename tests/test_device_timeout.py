@@ -24,13 +24,19 @@ import block_scaled_moe_topk_gb300 as moe
 import synth
 dev = torch.device("cuda", 0)
 s = synth.SHAPES["tiny"]
-T = 16
+T = int(sys.argv[3])
 W = synth.weights_codes(s.E, s.H, s.I, seed=0, device=dev)
+prepacked = sys.argv[4] == "1"
+if prepacked:
+    t1, t2 = torch.empty_like(W[1]), torch.empty_like(W[3])
+    moe.moe_prepack_scales(W[1], t1)
+    moe.moe_prepack_scales(W[3], t2)
+    W = (W[0], t1, W[2], t2)
 x, lg = synth.x_bf16(T, s.H, 0, device=dev), synth.gate_logits(T, s.E, 0, device=dev)
 out = torch.zeros(T, s.H, dtype=torch.bfloat16, device=dev)
 ws = torch.zeros(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=dev)
 t0 = time.time()
-moe.moe_forward_ex(x, lg, *W, out, s.E, s.k, ws, schedule=int(sys.argv[2]))
+moe.moe_forward_ex(x, lg, *W, out, s.E, s.k, ws, schedule=int(sys.argv[2]), weight_scales_prepacked=prepacked)
 torch.cuda.synchronize()
 dt = time.time() - t0
 status = moe.moe_read_device_status(ws)
@@ -40,24 +46,25 @@ print(json.dumps({"status": status, "words": words, "alive": alive, "seconds": d
 """
 
 
-@pytest.mark.parametrize("schedule", ["chain", "fused"])
+@pytest.mark.parametrize("schedule", ["chain", "fused", "split"])
 def test_expired_wait_is_reported_and_the_context_survives(schedule):
     import __graft_entry__
     __graft_entry__.build()
     env = dict(os.environ, MOE_TEST_STALL_PRODUCER="1", MOE_WAIT_TIMEOUT_NS="50000000")  # 50 ms
-    sched = {"chain": 1, "fused": 2}[schedule]
-    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(sched)], env=env, capture_output=True, text=True,
-                       timeout=600)
+    # split: T = 512 on the tiny shape with prepacked scales runs GEMM1 as the CTA-pair kernel
+    sched, T, pp = {"chain": (1, 16, 0), "fused": (2, 16, 0), "split": (1, 512, 1)}[schedule]
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(sched), str(T), str(pp)], env=env,
+                       capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     d = json.loads(r.stdout.strip().splitlines()[-1])
     assert d["status"] == 6  # MOE_ERR_DEVICE_TIMEOUT
     words = d["words"]
     assert words[1] == 1                 # an expiry was recorded
     # the first expiry: stage 0's full barrier in the MMA warp (index 0, warp 1) or the
-    # accumulator-ready barrier in an epilogue warp (index 2 * stages = 12: both schedules run a
-    # 6-stage ring for 16-row slots), warps 2-9, or -- fused schedule -- the combine's wait for
-    # every GEMM2 part in a CTA with no work of its own (1000 + its sync word offset 1),
-    # whichever came first
+    # accumulator-ready barrier in an epilogue warp (index 2 * stages = 12: the chain and fused
+    # schedules run a 6-stage ring for 16-row slots, the CTA-pair kernel a 6-stage ring), warps
+    # 2-9, or -- fused schedule -- the combine's wait for every GEMM2 part in a CTA with no work of
+    # its own (1000 + its sync word offset 1), whichever came first
     acc_ready = 12
     ok = (words[2], words[5]) == (0, 1) or (words[2] == acc_ready and 2 <= words[5] <= 9)
     if schedule == "fused":

@@ -330,6 +330,67 @@ def test_forward_entry_points_against_oracle(entry, shape, T, act):
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
 
 
+# --------------------------------------------------------------------------- split GEMMs
+# A8W4 with prepacked weight scales and T * k >= 128 * E: each GEMM runs as the pair kernel
+# (the experts' whole pairs of M tiles on CTA pairs) and the tail pass (each odd last M tile).
+def _forward_prepacked(x, lg, W, E, k, schedule):
+    T, H = x.shape
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(T, H, W.I, E, k), dtype=torch.uint8, device=DEV)
+    moe.moe_forward_ex(x.to(DEV), lg.to(DEV), *W.dev_prepacked(), out, E, k, ws, act_fmt=moe.MOE_ACT_MXFP8,
+                       weight_scales_prepacked=True, schedule=schedule)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    return out, ws
+
+
+@pytest.mark.parametrize("T,skew", [(512, False), (777, True), (2048, True)])
+def test_split_gemms_against_oracle_and_single_cta(T, skew):
+    """The tiny shape with its GEMMs split (skewed routing: experts with 1 to 4+ M tiles, odd
+    and even), the whole batch against the oracle and bit for bit against single-CTA tiles."""
+    E, k, H, I = TINY.E, TINY.k, TINY.H, TINY.I
+    assert moe.moe_forward_split_gemms(T, H, I, E, k, moe.MOE_ACT_MXFP8, moe.MOE_SCHEDULE_AUTO, True) == 3
+    W = Weights(E, H, I, seed=0, device=DEV, from_bf16=True)
+    x, lg = synth.x_bf16(T, H, 7), synth.gate_logits(T, E, 7, skew=skew)
+    out, ws = _forward_prepacked(x, lg, W, E, k, moe.MOE_SCHEDULE_AUTO)
+    ref, _ = _forward_prepacked(x, lg, W, E, k, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA)
+    assert torch.equal(out, ref)
+    counts = moe.workspace_views(ws, T, H, I, E, k)["counts"].cpu().numpy()
+    tiles = (counts + 127) // 128
+    assert (tiles % 2 == 1).any() and (tiles >= 2).any()  # both kernels had work
+    _check_intermediates(moe.MOE_ACT_MXFP8, x, lg, W, E, k, ws)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, oracle.FMT_E4M3)
+    rel, cos = compare(bits(out), want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape,T", [("pro", 8192), ("pro_skew", 8192), ("draft", 8192), ("pro", 16384)])
+def test_split_gemms_bit_identical_to_single_cta(shape, T):
+    """The benchmarked size and larger: the split GEMMs give the single-CTA tiles' bits."""
+    s = synth.SHAPES[shape]
+    assert moe.moe_forward_split_gemms(T, s.H, s.I, s.E, s.k, moe.MOE_ACT_MXFP8, moe.MOE_SCHEDULE_AUTO, True) == 3
+    W = _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 3), synth.gate_logits(T, s.E, 3, skew=s.skew)
+    out, _ = _forward_prepacked(x, lg, W, s.E, s.k, moe.MOE_SCHEDULE_AUTO)
+    ref, _ = _forward_prepacked(x, lg, W, s.E, s.k, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA)
+    assert torch.equal(out, ref)
+
+
+def test_profile_forward_names_split_gemms():
+    T, E, k, H, I = 512, TINY.E, TINY.k, TINY.H, TINY.I
+    W = Weights(E, H, I, seed=0, device=DEV)
+    x, lg = synth.x_bf16(T, H, 0).to(DEV), synth.gate_logits(T, E, 0).to(DEV)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(T, H, I, E, k), dtype=torch.uint8, device=DEV)
+    r = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *W.dev_prepacked(), out, E, k, ws, prepacked_scales=True)
+    assert list(r) == ["route", "scan", "scatter", "quant", "gemm1_pairs", "gemm1_tails", "gemm2_pairs",
+                       "gemm2_tails", "combine"]
+    assert all(v > 0 for v in r.values())
+    ref, _ = _forward_prepacked(x.cpu(), lg.cpu(), W, E, k, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA)
+    assert torch.equal(out, ref)
+
+
 # --------------------------------------------------------------------------- properties
 def test_forward_graph_replay_is_bit_identical():
     s = synth.SHAPES["flash_decode"]
