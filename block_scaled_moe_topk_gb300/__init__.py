@@ -48,7 +48,7 @@ class MoeError(RuntimeError):
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "sync", "topk_ids", "topk_w", "counts", "offsets", "padded_offsets", "mtile_base", "chunk_hist",
-        "sorted_pair", "inv", "inv_padded", "xq", "xs", "a2", "a2s", "y2", "part", "y2f", "total")] + [
+        "sorted_pair", "inv", "inv_padded", "xq", "xs", "a2", "a2s", "y2", "sf_rot", "part", "y2f", "total")] + [
         ("rows_cap", ctypes.c_int64), ("nchunk", ctypes.c_int64)]
 
 

@@ -95,6 +95,9 @@ moe_status_t layout(int64_t T, int H, int I, int E, int k, moe_act_fmt_t fmt, mo
   L->a2 = take(ib * rows_cap);
   L->a2s = take((size_t)I / 32 * rows_cap);
   L->y2 = take(sizeof(uint16_t) * (size_t)H * rows_cap);
+  // the split GEMMs' rotated A-scale atoms (only a batch the chain may split needs them)
+  const bool split_rows = moe::gemm_split_rows(T, E, k, fmt == MOE_ACT_MXFP8 ? 0 : 1);
+  L->sf_rot = take(split_rows ? (size_t)std::max(H, I) / 32 * rows_cap : 0);
   // the single-kernel decode schedule (T <= 64): partial accumulators and fp32 GEMM2 rows
   const bool decode = T <= moe::kDecodeMaxTokens;
   L->part = take(decode ? moe::decode_part_bytes(T) : 0);
@@ -164,7 +167,7 @@ int gemm_a_rows(int64_t T, int E, int k, int K) {
 // plus the tail pass (moe::gemm_pair_split).
 bool split_gemm(int64_t T, int E, int k, int afmt, bool prepacked, int schedule, int N, int K) {
   if (schedule == MOE_SCHEDULE_CHAIN_SINGLE_CTA || schedule == MOE_SCHEDULE_CHAIN_BF16_H) return false;
-  return moe::gemm_pair_split(T, E, k, afmt, prepacked, N, gemm_a_rows(T, E, k, K));
+  return moe::gemm_pair_split(T, E, k, afmt, prepacked, N, K, gemm_a_rows(T, E, k, K));
 }
 int launch_count_cfg(int64_t T, int H, int I, int E, int k, int afmt, int schedule, bool prepacked) {
   const int n = launch_count(T, H, I, schedule);
@@ -314,13 +317,18 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   auto a_rows_for = [&](int K) { return gemm_a_rows(T, E, k, K); };
   g1.a_rows = a_rows_for(H);
   // a GEMM, split into the pair kernel and the tail pass where that pays (split_gemm)
+  // (the tail pass on CTA pairs, 512 columns a pair tile, when N allows: its odd CTAs read the
+  // rotated A-scale atoms the pair kernel writes to sf_rot)
   auto run_gemm = [&](const moe::GemmArgs& g) -> cudaError_t {
     if (g.epilogue != 2 && split_gemm(T, E, k, afmt, tiled_scales, schedule, g.N, g.K)) {
-      cudaError_t e = moe::launch_gemm_pair(g, s);
+      moe::GemmArgs t = g;
+      const bool wide = moe::gemm_tail_wide(g.N, g.K);
+      t.act_sf_rot = wide ? at(L.sf_rot) : nullptr;
+      cudaError_t e = moe::launch_gemm_pair(t, s);
       if (e != cudaSuccess) return e;
       e = mark();
       if (e != cudaSuccess) return e;
-      moe::GemmArgs t = g;
+      if (wide) return moe::launch_gemm_tail_wide(t, s);
       t.tail_only = 1;
       return moe::launch_gemm(t, s);
     }

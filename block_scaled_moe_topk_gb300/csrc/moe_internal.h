@@ -130,6 +130,9 @@ struct GemmArgs {
                           // 16 requires every tile to hold at most 16 routed rows)
   int tail_only;          // single-CTA tiles, A8W4, 128 rows: only each expert's odd last M tile
                           // (after launch_gemm_pair took the whole pairs)
+  uint8_t* act_sf_rot;    // split GEMMs with the wide tail pass: launch_gemm_pair writes the A-scale
+                          // atoms of each expert's odd last M tile here, halves swapped, for
+                          // launch_gemm_tail_wide (same layout as act_sf); null otherwise
 };
 // Single-CTA GEMMs stage 16 activation rows when T <= 16, and 64 rows (in 64-row work units)
 // when the batch routes at most this many rows per expert on average (T * k <= 16 * E) and the
@@ -142,15 +145,37 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 // gemm_pair.cu: the whole pairs of each expert's M tiles on CTA pairs (prepacked weight scales,
 // N a multiple of 256); gemm.cu's tail pass (tail_only) then takes each odd last M tile.
 cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t s);
-// The kernel chain splits a GEMM into the pair kernel and the tail pass when its tiles are the
-// 128-row A8W4 ones, the weight scales are prepacked, N is a multiple of 256, and the batch
-// routes at least kPairMinRowsPerExpert rows per expert on average (then about half the
-// experts or more have a second M tile): measured on V4-Pro A8W4, GEMM1 -8.7 % and GEMM2 -6.8 %
-// at T = 8192, -4.7 % / -3 % at T = 16384, equal at T = 32768.
+// gemm_pair.cu: the tail pass of a split GEMM on CTA pairs (cta_group::2, M = 128), each pair
+// tile an expert's odd last M tile by 512 output columns (N a multiple of 512), reading the
+// rotated A-scale atoms launch_gemm_pair wrote to act_sf_rot.  Five 43 KiB stages keep 80 KiB of
+// weight bytes in flight per SM, against 64 KiB for the single-CTA tail tiles.
+constexpr int kTailWideN = 2 * kNTile;
+cudaError_t launch_gemm_tail_wide(const GemmArgs& a, cudaStream_t s);
+// The wide tail pass serves GEMMs with N a multiple of 512 and at least kTailWideMinStages K
+// stages: with short K (V4.1-Flash and draft GEMM2, 5-9 stages a tile) the accumulator hand-off
+// between tiles and the pair kernel's fixed cost outweighed the deeper ring (+6 to +20 % for
+// those layers at T = 1024-8192).
+constexpr int kTailWideMinStages = 16;
+inline bool gemm_tail_wide(int N, int K) { return N % kTailWideN == 0 && K / 128 >= kTailWideMinStages; }
+// The kernel chain splits a GEMM into the pair kernel and a tail pass when its tiles are the
+// 128-row A8W4 ones, the weight scales are prepacked and N is a multiple of 256, and
+//   * its tail pass is the wide one and the batch routes more than kUnit64MaxRowsPerExpert rows
+//     per expert on average: measured on V4-Pro A8W4 against single-CTA tiles throughout, -7 to
+//     -9 % for the layer at T = 1025-6144, and at T = 8192 GEMM1 / GEMM2 tails 860 / 460 ->
+//     779 / 440 us; or
+//   * the batch routes at least kPairMinRowsPerExpert rows per expert on average (then about
+//     half the experts or more have a second M tile): with the single-CTA tail pass, GEMM1
+//     -8.7 % and GEMM2 -6.8 % at T = 8192, -4.7 % / -3 % at T = 16384, equal at T = 32768.
 constexpr int kPairMinRowsPerExpert = 128;
-inline bool gemm_pair_split(int64_t T, int E, int k, int act_fmt, bool prepacked, int N, int a_rows) {
-  return act_fmt == 0 && prepacked && N % kNTile == 0 && a_rows == kRowTile &&
-         T * (int64_t)k >= (int64_t)kPairMinRowsPerExpert * E;
+inline bool gemm_pair_split(int64_t T, int E, int k, int act_fmt, bool prepacked, int N, int K, int a_rows) {
+  if (act_fmt != 0 || !prepacked || N % kNTile != 0 || a_rows != kRowTile) return false;
+  const int64_t rows = T * (int64_t)k;
+  return rows >= (int64_t)kPairMinRowsPerExpert * E ||
+         (gemm_tail_wide(N, K) && rows > (int64_t)kUnit64MaxRowsPerExpert * E);
+}
+// Whether a batch may split a GEMM with the wide tail pass (the workspace then holds sf_rot).
+inline bool gemm_split_rows(int64_t T, int E, int k, int act_fmt) {
+  return act_fmt == 0 && T * (int64_t)k > (int64_t)kUnit64MaxRowsPerExpert * E;
 }
 
 

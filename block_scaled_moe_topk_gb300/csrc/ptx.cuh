@@ -271,6 +271,11 @@ __device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64
 // M = 256 block-scaled MMAs over the pair: A rows [0,128) from the even CTA's shared memory,
 // [128,256) from the odd CTA's; the N rows of B split the same way; each CTA's TMEM receives
 // the accumulator rows of its own A rows.
+// Copy of 64 rows x 128 bits, rows 0-31 to lane quadrants 0 and 1, rows 32-63 to quadrants 2
+// and 3 (warpx2::01_23), on a CTA pair.
+__device__ __forceinline__ void tc_cp_pair_64x128b_warpx2_0123(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.64x128b.warpx2::01_23 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 __device__ __forceinline__ void tc_mma_pair_mxf8f6f4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                      uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
   asm volatile(

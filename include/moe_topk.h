@@ -151,6 +151,9 @@ const char* moe_status_string(moe_status_t status);
  *   y2           bf16 [rows_cap, H]        GEMM2 output rows (unweighted; fp32-accumulated,
  *                                          rounded to bf16 like the pages' reduced-precision
  *                                          stage-2 transport)
+ *   sf_rot       u8 [rows_cap/128][max(H, I)/128][512]  scratch of the split GEMMs: the A-scale
+ *                atoms of each expert's odd last M tile with their two 64-row halves swapped
+ *                (GEMM1's, then GEMM2's); empty unless A8W4 and T * k >= 128 * E
  *   part         fp32 partial accumulators of the fused schedule (T <= 64 only, else empty)
  *   y2f          fp32 [T*k, H] GEMM2 rows of the fused schedule, unpadded row order
  *                (T <= 64 only, else empty)
@@ -165,7 +168,7 @@ const char* moe_status_string(moe_status_t status);
  */
 typedef struct {
   size_t status, sync, topk_ids, topk_w, counts, offsets, padded_offsets, mtile_base, chunk_hist;
-  size_t sorted_pair, inv, inv_padded, xq, xs, a2, a2s, y2, part, y2f;
+  size_t sorted_pair, inv, inv_padded, xq, xs, a2, a2s, y2, sf_rot, part, y2f;
   size_t total;      /* bytes needed == moe_workspace_bytes(...) */
   int64_t rows_cap;  /* padded row capacity (multiple of 128) */
   int64_t nchunk;    /* number of routing chunks (sort scratch width) */

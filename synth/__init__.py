@@ -48,6 +48,8 @@ class Shape:
 
 SHAPES = {
     "tiny": Shape("tiny", 256, 128, 8, 2),
+    # both GEMMs' N (2I, H) multiples of 512 and K (H, I) of 16 stages: the wide tail pass
+    "tiny_wide": Shape("tiny_wide", 2048, 2048, 8, 2),
     "flash_decode": Shape("flash_decode", 5120, 640, 384, 6),
     "draft": Shape("draft", 5120, 1152, 128, 3, skew=True),
     "pro": Shape("pro", 7168, 3072, 384, 6),

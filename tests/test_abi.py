@@ -46,9 +46,10 @@ def test_workspace_layout_and_bytes():
     R = 8192 * 6
     assert L.rows_cap % 128 == 0 and L.rows_cap >= R and L.rows_cap <= R + 127 * 384 + 127
     offs = [L.status, L.sync, L.topk_ids, L.topk_w, L.counts, L.offsets, L.padded_offsets, L.mtile_base,
-            L.chunk_hist, L.sorted_pair, L.inv, L.inv_padded, L.xq, L.xs, L.a2, L.a2s, L.y2, L.part, L.y2f]
+            L.chunk_hist, L.sorted_pair, L.inv, L.inv_padded, L.xq, L.xs, L.a2, L.a2s, L.y2, L.sf_rot, L.part, L.y2f]
     assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
-    assert L.y2 + 2 * 7168 * L.rows_cap <= L.total  # bf16 GEMM2 rows
+    assert L.y2 + 2 * 7168 * L.rows_cap <= L.sf_rot  # bf16 GEMM2 rows
+    assert L.sf_rot + 7168 // 32 * L.rows_cap <= L.total  # rotated A-scale atoms of the split GEMMs
     assert L.part == L.y2f == L.total  # the fused schedule's buffers exist only for T <= 64
     assert L.sync == 256  # right after the status words (one memset clears both)
     small = moe.moe_get_workspace_layout(64, 7168, 3072, 384, 6)
@@ -56,7 +57,9 @@ def test_workspace_layout_and_bytes():
     assert small.total - small.y2f >= 64 * 6 * 7168 * 4      # fp32 GEMM2 rows
     assert moe.moe_workspace_bytes(8192, 7168, 3072, 384, 6) == L.total
     a4 = moe.moe_get_workspace_layout(8192, 7168, 3072, 384, 6, moe.MOE_ACT_MXFP4)
-    assert a4.total < L.total
+    assert a4.total < L.total and a4.part == a4.sf_rot  # A4W4 never splits: no rotated scales
+    few = moe.moe_get_workspace_layout(1024, 7168, 3072, 384, 6)
+    assert few.part == few.sf_rot  # at most 16 rows per expert on average: 64-row units, no split
     # rows_cap never exceeds R + 127 per active expert: T=1 routes to k experts
     L1 = moe.moe_get_workspace_layout(1, 7168, 3072, 384, 6)
     assert L1.rows_cap == 6 * 128
@@ -123,13 +126,24 @@ def test_forward_launch_count():
 
 def test_forward_launch_count_with_split_gemms():
     """The exact count: a GEMM split into its pair kernel and tail pass (A8W4, prepacked scales,
-    128-row tiles, N % 256 == 0, T * k >= 128 * E) counts twice."""
+    128-row tiles, N % 256 == 0, and N % 512 == 0 with T * k > 16 * E or T * k >= 128 * E) counts
+    twice."""
     pro, a8, a4 = (7168, 3072), moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4
     auto, chain = moe.MOE_SCHEDULE_AUTO, moe.MOE_SCHEDULE_CHAIN
     cfg, split = moe.moe_forward_launch_count_cfg, moe.moe_forward_split_gemms
     assert (cfg(8192, *pro, 384, 6, a8, auto, True), split(8192, *pro, 384, 6, a8, auto, True)) == (9, 3)
     assert (cfg(8192, *pro, 384, 6, a8, chain, True), split(8192, *pro, 384, 6, a8, chain, True)) == (9, 3)
-    assert (cfg(8191, *pro, 384, 6, a8, auto, True), split(8191, *pro, 384, 6, a8, auto, True)) == (7, 0)  # < 128 rows / expert
+    assert (cfg(8191, *pro, 384, 6, a8, auto, True), split(8191, *pro, 384, 6, a8, auto, True)) == (9, 3)  # wide tails
+    assert (cfg(1025, *pro, 384, 6, a8, auto, True), split(1025, *pro, 384, 6, a8, auto, True)) == (9, 3)
+    assert (cfg(1024, *pro, 384, 6, a8, auto, True), split(1024, *pro, 384, 6, a8, auto, True)) == (7, 0)  # 64-row units
+    # V4.1-Flash (5120/640): GEMM1's N = 1280 is no multiple of 512 and GEMM2's K = 640 is 5 stages,
+    # so neither takes the wide tails: both split from 128 rows per expert on; the draft shape's GEMM1
+    # (N = 2304, K = 5120) neither; GEMM2 of I = 2048 (K = 16 stages) does
+    flash, draft = (5120, 640), (5120, 1152)
+    assert (cfg(2048, *flash, 384, 6, a8, auto, True), split(2048, *flash, 384, 6, a8, auto, True)) == (7, 0)
+    assert split(8192, *flash, 384, 6, a8, auto, True) == 3
+    assert split(2048, *draft, 128, 3, a8, auto, True) == 0
+    assert split(2048, 5120, 2048, 128, 3, a8, auto, True) == 3
     assert cfg(8192, *pro, 384, 6, a8, auto, False) == 7                     # canonical weight scales
     assert cfg(8192, *pro, 384, 6, a4, auto, True) == 7                      # A4W4
     assert cfg(8192, *pro, 384, 6, a8, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA, True) == 7

@@ -23,7 +23,7 @@ import torch
 import block_scaled_moe_topk_gb300 as moe
 import synth
 dev = torch.device("cuda", 0)
-s = synth.SHAPES["tiny"]
+s = synth.SHAPES[sys.argv[5]]
 T = int(sys.argv[3])
 W = synth.weights_codes(s.E, s.H, s.I, seed=0, device=dev)
 prepacked = sys.argv[4] == "1"
@@ -46,14 +46,16 @@ print(json.dumps({"status": status, "words": words, "alive": alive, "seconds": d
 """
 
 
-@pytest.mark.parametrize("schedule", ["chain", "fused", "split"])
+@pytest.mark.parametrize("schedule", ["chain", "fused", "split", "split_wide"])
 def test_expired_wait_is_reported_and_the_context_survives(schedule):
     import __graft_entry__
     __graft_entry__.build()
     env = dict(os.environ, MOE_TEST_STALL_PRODUCER="1", MOE_WAIT_TIMEOUT_NS="50000000")  # 50 ms
     # split: T = 512 on the tiny shape with prepacked scales runs GEMM1 as the CTA-pair kernel
-    sched, T, pp = {"chain": (1, 16, 0), "fused": (2, 16, 0), "split": (1, 512, 1)}[schedule]
-    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(sched), str(T), str(pp)], env=env,
+    # split_wide: the same on tiny_wide (N = 512), whose tail pass is the wide CTA-pair kernel
+    sched, T, pp, shape = {"chain": (1, 16, 0, "tiny"), "fused": (2, 16, 0, "tiny"), "split": (1, 512, 1, "tiny"),
+                           "split_wide": (1, 512, 1, "tiny_wide")}[schedule]
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(sched), str(T), str(pp), shape], env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     d = json.loads(r.stdout.strip().splitlines()[-1])
