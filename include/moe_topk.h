@@ -89,11 +89,14 @@ typedef enum {
  *   MOE_SCHEDULE_CHAIN  the kernel chain: routing + sort, quantiser, GEMM1, GEMM2, combine;
  *                       each GEMM runs one CTA per 128-row x 256-column tile over the whole K;
  *                       GEMM2 rows are stored as bf16 before the combine.  With A8W4,
- *                       prepacked weight scales, 128-row tiles, an N (2I for GEMM1, H for GEMM2)
- *                       that is a multiple of 256 and T * k >= 128 * E, a GEMM runs as two
- *                       kernels: the experts' whole pairs of M tiles on CTA pairs
- *                       (cta_group::2), then each expert's odd last M tile on single CTAs
- *                       (bit-identical to CHAIN_SINGLE_CTA, faster at large T).
+ *                       prepacked weight scales, 128-row tiles and an N (2I for GEMM1, H for
+ *                       GEMM2) that is a multiple of 256, a GEMM runs as two kernels -- the
+ *                       experts' whole pairs of M tiles on CTA pairs (cta_group::2), then a tail
+ *                       pass over each expert's odd last M tile -- when either
+ *                         N is a multiple of 512, K (H for GEMM1, I for GEMM2) at least 2048 and
+ *                         T * k > 16 * E: the tail pass runs 512-column tiles on CTA pairs; or
+ *                         T * k >= 128 * E: otherwise the tail pass runs on single CTAs.
+ *                       Bit-identical to CHAIN_SINGLE_CTA, and faster.
  *   MOE_SCHEDULE_CHAIN_SINGLE_CTA  the kernel chain with single-CTA GEMM tiles throughout.
  *   MOE_SCHEDULE_FUSED  T <= 64 and H <= 16384 only (else MOE_ERR_UNSUPPORTED_SHAPE): the whole layer in one
  *                       persistent kernel on every SM ("feat(moe): FlyDSL MegaMoE fused EP-MoE
@@ -153,7 +156,7 @@ const char* moe_status_string(moe_status_t status);
  *                                          stage-2 transport)
  *   sf_rot       u8 [rows_cap/128][max(H, I)/128][512]  scratch of the split GEMMs: the A-scale
  *                atoms of each expert's odd last M tile with their two 64-row halves swapped
- *                (GEMM1's, then GEMM2's); empty unless A8W4 and T * k >= 128 * E
+ *                (GEMM1's, then GEMM2's); empty unless A8W4 and T * k > 16 * E
  *   part         fp32 partial accumulators of the fused schedule (T <= 64 only, else empty)
  *   y2f          fp32 [T*k, H] GEMM2 rows of the fused schedule, unpadded row order
  *                (T <= 64 only, else empty)
