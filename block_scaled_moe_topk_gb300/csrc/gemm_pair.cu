@@ -11,17 +11,18 @@
 // output columns, computed by a cluster of two CTAs on two SMs with tcgen05.mma.cta_group::2
 // (M = 256):
 //   * each CTA loads its own 128 activation rows and 128 of the 256 weight rows of the tile,
-//     so a CTA's shared-memory stage is 35 KiB instead of 50 KiB: the ring is 6 deep, which
-//     covers the load latency better than the single kernel's 4 stages;
+//     through two rings: 5 stages of activation rows and 8 of weight rows (16 KiB of shared
+//     memory each), against the single kernel's 4 stages of 50 KiB holding both;
 //   * each CTA stages the scales of all 256 weight rows of the tile (the MMA of each SM reads
 //     the weight scales of every output column from its own TMEM);
 //   * one elected lane of the even CTA's converged MMA warp issues the scale copies to TMEM and
-//     the MMAs for both; each CTA's TMEM receives the accumulator of its own 128 rows;
-//   * every TMA load of either CTA completes on the even CTA's "full" barrier, whose expected
-//     byte count the even CTA's producers post for both CTAs (local arrivals only: a remote
-//     arrive with release semantics stalls the issuing thread on a cluster-wide fence); the MMA
-//     commit releases the slot in both CTAs (multicast), and the accumulator hand-off goes to
-//     both epilogues, whose "TMEM free" arrivals go back to the even CTA.
+//     the MMAs for both, once a stage's slots of both rings are full; each CTA's TMEM receives
+//     the accumulator of its own 128 rows;
+//   * every TMA load of either CTA completes on the even CTA's "full" barrier of its ring, whose
+//     expected byte count the even CTA's producer posts for both CTAs (local arrivals only: a
+//     remote arrive with release semantics stalls the issuing thread on a cluster-wide fence);
+//     the MMA commits release the stage's slots in both CTAs (multicast), and the accumulator
+//     hand-off goes to both epilogues, whose "TMEM free" arrivals go back to the even CTA.
 // Measured (V4-Pro A8W4, T = 8192): a pair stage costs ~0.32 us per SM against ~0.42 for the
 // single kernel's, so the pairs plus the tail pass run GEMM1 in 1.94 ms against 2.13 ms for
 // single-CTA tiles throughout.
@@ -41,25 +42,34 @@
 namespace moe {
 namespace {
 
-constexpr int kPStages = 6;
+// Two rings: activation tiles (with their scale atom) and weight tiles (with theirs), each with
+// its own full / empty barriers, so the weight ring can be deeper than the activation ring:
+// the weight stream, which nothing else reads, is bound by its bytes in flight per SM (~2 us of
+// loaded latency), and a CTA's activation tile (16 KiB a stage, mostly L2 hits: the expert's
+// other N tiles read it too) would otherwise take as many slots.
+constexpr int kPStagesA = 5;                       // activation ring
+constexpr int kPStagesW = 8;                       // weight ring: 8 x 8 KiB of weights in flight
 constexpr int kPThreads = 352;
 constexpr int kPEpiWarps = 8;
 constexpr int kPBWarp = 10;
 constexpr int kPHalfRows = 128;                    // weight rows per CTA (half of kNTile)
 constexpr int kPABytes = kRowTile * 128;           // 128 activation rows x 128 bytes
 constexpr int kPBBytes = kPHalfRows * 128;         // 128 weight rows x 128 bytes (smem footprint)
-constexpr int kPSfaOff = kPABytes + kPBBytes;
-constexpr int kPSfbOff = kPSfaOff + 1024;
-constexpr int kPStageBytes = kPSfbOff + 2048;      // 35 KiB, a multiple of 1024
-constexpr int kPBarOff = kPStages * kPStageBytes;
+constexpr int kPWOff = kPStagesA * kPABytes;       // the weight ring after the activation ring
+constexpr int kPSfaOff = kPWOff + kPStagesW * kPBBytes;   // activation-scale atoms, 512 B a slot
+constexpr int kPSfbOff = kPSfaOff + kPStagesA * 512;      // weight-scale atoms, 2 x 512 B a slot
+constexpr int kPBarOff = kPSfbOff + kPStagesW * 1024;
 constexpr int kPBaseOff = kPBarOff + 256;          // pair-tile prefix over experts, int32 [E+1]
-constexpr int kPTileBaseOff = kPBaseOff + 4 * (kMaxExperts + 1);  // M-tile prefix, int32 [E+1]
-constexpr int kPSmemBytes = kPTileBaseOff + 4 * (kMaxExperts + 1) + 1024;
+constexpr int kPSmemBytes = kPBaseOff + 4 * (kMaxExperts + 1) + 1024;
 constexpr uint32_t kPTmemCols = 512;
-constexpr uint32_t kPSfCol0 = 256;
-constexpr uint32_t kPSfSlotCols = 32;
+constexpr uint32_t kPSfCol0 = 256;                 // accumulator: columns [0, 256)
+constexpr uint32_t kPSfSlotCols = 12;              // 4 A-scale + 8 weight-scale columns
 static_assert(kPSmemBytes <= 232448, "pair GEMM shared memory");
-static_assert(kPStages * kPSfSlotCols <= kPTmemCols - kPSfCol0, "pair GEMM TMEM scale slots");
+static_assert(kPWOff % 1024 == 0 && kPSfaOff % 1024 == 0, "pair GEMM ring alignment");
+static_assert(8 * (2 * kPStagesA + 2 * kPStagesW + 3) + 8 <= 256, "pair GEMM barriers");
+// TMEM scale slots follow the activation ring: the copy for stage i + kPStagesA is issued only
+// after the activation slot of stage i was released, i.e. after stage i's MMAs completed.
+static_assert(kPSfCol0 + kPStagesA * kPSfSlotCols <= kPTmemCols, "pair GEMM TMEM scale slots");
 
 struct PairParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_act;  // activation codes [rows_cap, K or K/2], box 128 B x 128 rows
@@ -110,26 +120,28 @@ __device__ __noinline__ void grace_spin(uint64_t cycles) {
 
 template <int ACT, int EPI>
 __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __grid_constant__ PairParams p) {
+  static_assert(ACT == 0, "the pair kernel serves A8W4 (E4M3 x E2M1)");
   using TR = ActTraits<ACT>;
   constexpr int kMmaPerStage = TR::kKPerStage / TR::kMmaK;  // 4
-  constexpr int kAtomsPerStage = TR::kKPerStage / 128;      // k-atoms of 4 scale blocks
-  constexpr uint32_t kSfaCols = kAtomsPerStage * 4;
-  constexpr uint32_t kScaleBoxBytes = kAtomsPerStage * 512;
+  constexpr uint32_t kSfaCols = 4;
+  constexpr uint32_t kScaleBoxBytes = 512;                  // one k-atom a stage
   constexpr uint32_t kBHalfTx = TR::kBTxBytes / 2;          // global bytes of 128 weight rows
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + kPBarOff;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kPStages + s); };
-  const uint32_t tmem_full_bar = bar0 + 8u * (2 * kPStages);
+  auto full_a = [&](int s) { return bar0 + 8u * s; };
+  auto empty_a = [&](int s) { return bar0 + 8u * (kPStagesA + s); };
+  auto full_w = [&](int s) { return bar0 + 8u * (2 * kPStagesA + s); };
+  auto empty_w = [&](int s) { return bar0 + 8u * (2 * kPStagesA + kPStagesW + s); };
+  const uint32_t tmem_full_bar = bar0 + 8u * (2 * kPStagesA + 2 * kPStagesW);
   const uint32_t tmem_empty_bar = tmem_full_bar + 8;
   const uint32_t drain_bar = tmem_full_bar + 16;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kPBarOff + 8 * (2 * kPStages + 3));
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kPBarOff + 8 * (2 * kPStagesA + 2 * kPStagesW + 3));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int32_t* pair_base = reinterpret_cast<int32_t*>(smem + kPBaseOff);
-  int32_t* tile_base = reinterpret_cast<int32_t*>(smem + kPTileBaseOff);
+  const int32_t* tile_base = p.mtile_base;  // M-tile prefix (read once per tile)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
@@ -137,9 +149,13 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
   const int E = p.E;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPStages; ++s) {
-      mbar_init(full_bar(s), 2);    // expect_tx arrivals of warps 0 and 10 of the even CTA
-      mbar_init(empty_bar(s), 1);   // the pair's MMA commit
+    for (int s = 0; s < kPStagesA; ++s) {
+      mbar_init(full_a(s), 1);      // expect_tx arrival of warp 0 of the even CTA
+      mbar_init(empty_a(s), 1);     // the pair's MMA commit
+    }
+    for (int s = 0; s < kPStagesW; ++s) {
+      mbar_init(full_w(s), 1);      // expect_tx arrival of warp 10 of the even CTA
+      mbar_init(empty_w(s), 1);
     }
     mbar_init(tmem_full_bar, 1);
     mbar_init(tmem_empty_bar, 2 * kPEpiWarps);  // epilogue warps of both CTAs
@@ -147,9 +163,7 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // Expert tile prefixes in shared memory (the per-tile lookups sit on the producers' path):
-  // M tiles as given, and pair tiles per expert, ceil(M tiles / 2), prefixed by warp 2.
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) tile_base[e] = p.mtile_base[e];
+  // Pair tiles per expert (whole pairs of M tiles), prefixed by warp 2 into shared memory.
   if (warp == 2) {
     int running = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -182,11 +196,12 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
   const int64_t total_tiles = (int64_t)pair_base[E] * NT;
   const int64_t first_tile = cluster_index();
   const int64_t tile_step = cluster_count();
-  const uint32_t leader_full0 = mapa_shared(full_bar(0), 0);
-
   if (warp == 0 || warp == kPBWarp) {
     // ------------------------------------------------------------------ producers (converged)
     const bool act_warp = warp == 0;
+    const int depth = act_warp ? kPStagesA : kPStagesW;
+    // the even CTA's barriers of this producer's ring
+    const uint32_t lfull0 = mapa_shared(act_warp ? full_a(0) : full_w(0), 0);
     {
       int slot = 0;
       uint32_t phase = 0;
@@ -208,29 +223,30 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
         const uint32_t act_tx = ((uint32_t)kPABytes + kScaleBoxBytes) * (peer_real ? 2u : 1u);
         const uint32_t w_tx = 2u * (kBHalfTx + 2u * kScaleBoxBytes);
         for (int ks = 0; ks < nks; ++ks) {
-          if (!warp_wait(empty_bar(slot), phase ^ 1u, sync, p.timeout_ns)) {
+          if (!warp_wait(act_warp ? empty_a(slot) : empty_w(slot), phase ^ 1u, sync, p.timeout_ns)) {
             ok = false;
             break;
           }
-          const uint32_t st = sbase + (uint32_t)slot * kPStageBytes;
-          const uint32_t lfull = leader_full0 + 8u * slot;
-          const int ky = 2 * ks * kAtomsPerStage;
+          const uint32_t lfull = lfull0 + 8u * slot;
+          const int ky = 2 * ks;
           if (elect_one()) {
             if (act_warp) {
-              if (leader) mbar_arrive_expect_tx(full_bar(slot), act_tx);
+              if (leader) mbar_arrive_expect_tx(full_a(slot), act_tx);
               if (real) {
-                tma_load_2d_pair(st, &p.tmap_act, lfull, ks * 128, (int)row0);
-                tma_load_2d_pair(st + kPSfaOff, &p.tmap_asf, lfull, 0, asf_y0 + ky);
+                tma_load_2d_pair(sbase + (uint32_t)slot * kPABytes, &p.tmap_act, lfull, ks * 128, (int)row0);
+                tma_load_2d_pair(sbase + kPSfaOff + (uint32_t)slot * 512u, &p.tmap_asf, lfull, 0, asf_y0 + ky);
               }
             } else {
-              if (leader) mbar_arrive_expect_tx(full_bar(slot), w_tx);
-              tma_load_3d_pair(st + kPABytes, &p.tmap_w, lfull, ks * 128, n0 + (int)rank * kPHalfRows, pt.e);
-              tma_load_2d_pair(st + kPSfbOff, &p.tmap_wsf, lfull, 0, wsf_y0 + ky);
-              tma_load_2d_pair(st + kPSfbOff + kScaleBoxBytes, &p.tmap_wsf, lfull, 0, wsf_y0 + wsf_half + ky);
+              if (leader) mbar_arrive_expect_tx(full_w(slot), w_tx);
+              const uint32_t sfb = sbase + kPSfbOff + (uint32_t)slot * 1024u;
+              tma_load_3d_pair(sbase + kPWOff + (uint32_t)slot * kPBBytes, &p.tmap_w, lfull, ks * 128,
+                               n0 + (int)rank * kPHalfRows, pt.e);
+              tma_load_2d_pair(sfb, &p.tmap_wsf, lfull, 0, wsf_y0 + ky);
+              tma_load_2d_pair(sfb + kScaleBoxBytes, &p.tmap_wsf, lfull, 0, wsf_y0 + wsf_half + ky);
             }
           }
           __syncwarp();
-          if (++slot == kPStages) {
+          if (++slot == depth) {
             slot = 0;
             phase ^= 1u;
           }
@@ -243,17 +259,17 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
     // The warp runs the loop converged and one elected lane issues each tcgen05.cp / mma /
     // commit (see gemm.cu), with every descriptor and TMEM address precomputed.
     if (leader) {
-      int slot = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int sa = 0, sw = 0;             // activation and weight ring slots
+      uint32_t pa = 0, pw = 0, acc_phase = 0;
       bool ok = true, issued = false;
-      // descriptors of slot 0; a slot adds kPStageBytes, an MMA step 32 bytes (start address
-      // field, in 16-byte units; shared-memory offsets stay below 2^18, so no carry)
+      // descriptors of slot 0 of each ring; a slot adds its bytes, an MMA step 32 bytes (start
+      // address field, in 16-byte units; shared-memory offsets stay below 2^18, so no carry)
       const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kLayoutSwizzle128B);
-      const uint64_t b_desc0 = smem_desc(sbase + kPABytes, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(sbase + kPWOff, 16, 1024, kLayoutSwizzle128B);
       const uint64_t sfa_desc0 = smem_desc(sbase + kPSfaOff, 128, 128, kLayoutNone);
       const uint64_t sfb_desc0 = smem_desc(sbase + kPSfbOff, 128, 128, kLayoutNone);
-      constexpr uint64_t kSlotStep = kPStageBytes >> 4;
-      constexpr uint32_t kSfbCols = 8;  // TMEM columns of the 256 weight rows' scales per k-atom
+      constexpr uint64_t kAStep = kPABytes >> 4, kBStep = kPBBytes >> 4;
+      constexpr uint32_t kSfbCols = 8;  // TMEM columns of the 256 weight rows' scales
       for (int64_t tile = first_tile; ok && tile < total_tiles; tile += tile_step) {
         if (!warp_wait(tmem_empty_bar, acc_phase ^ 1u, sync, p.timeout_ns)) {
           ok = false;
@@ -261,64 +277,36 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
         }
         tc_fence_after();
         for (int ks = 0; ks < nks; ++ks) {
-          if (!warp_wait(full_bar(slot), phase, sync, p.timeout_ns)) {
+          if (!warp_wait(full_a(sa), pa, sync, p.timeout_ns) || !warp_wait(full_w(sw), pw, sync, p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t so = (uint64_t)slot * kSlotStep;
-          const uint32_t sf_col = tmem_base + kPSfCol0 + (uint32_t)slot * kPSfSlotCols;
-          const int kvalid = min(TR::kKPerStage, K - ks * TR::kKPerStage);
-          const bool el = elect_one();
-          if (el && kvalid == TR::kKPerStage) {
-#pragma unroll
-            for (int ka = 0; ka < kAtomsPerStage; ++ka) {
-              tc_cp_pair_32x128b_warpx4(sf_col + ka * 4, sfa_desc0 + so + ka * 32);
-              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols, sfb_desc0 + so + ka * 32);
-              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols + 4,
-                                        sfb_desc0 + so + (kScaleBoxBytes >> 4) + ka * 32);
-            }
+          const uint64_t ao = (uint64_t)sa * kAStep, bo = (uint64_t)sw * kBStep;
+          const uint32_t sf_col = tmem_base + kPSfCol0 + (uint32_t)sa * kPSfSlotCols;
+          if (elect_one()) {
+            tc_cp_pair_32x128b_warpx4(sf_col, sfa_desc0 + (uint64_t)sa * 32);
+            tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols, sfb_desc0 + (uint64_t)sw * 64);
+            tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + 4, sfb_desc0 + (uint64_t)sw * 64 + (kScaleBoxBytes >> 4));
 #pragma unroll
             for (int j = 0; j < kMmaPerStage; ++j) {
-              constexpr int kBlkPerMma = TR::kMmaK / 32;
-              const int kblk = j * kBlkPerMma;
-              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3), 2 * kRowTile);
-              const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
-              if (ACT == 0)
-                tc_mma_pair_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
-                                     sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
-              else
-                tc_mma_pair_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
-                                 sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
+              const uint32_t idesc = make_idesc<ACT>((uint32_t)j, 2 * kRowTile);
+              tc_mma_pair_mxf8f6f4(tmem_base, a_desc0 + ao + 2 * j, b_desc0 + bo + 2 * j, idesc, sf_col,
+                                   sf_col + kSfaCols, (ks > 0 || j > 0) ? 1u : 0u);
             }
-          } else if (el) {
-            // the last stage of a K that is not a multiple of the stage depth (A4W4: one k-atom)
-            const int katoms = kvalid / 128;
-            const int nmma = kvalid / TR::kMmaK;
-            for (int ka = 0; ka < katoms; ++ka) {
-              tc_cp_pair_32x128b_warpx4(sf_col + ka * 4, sfa_desc0 + so + ka * 32);
-              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols, sfb_desc0 + so + ka * 32);
-              tc_cp_pair_32x128b_warpx4(sf_col + kSfaCols + ka * kSfbCols + 4,
-                                        sfb_desc0 + so + (kScaleBoxBytes >> 4) + ka * 32);
-            }
-            for (int j = 0; j < nmma; ++j) {
-              const int kblk = j * (TR::kMmaK / 32);
-              const uint32_t idesc = make_idesc<ACT>((uint32_t)(kblk & 3), 2 * kRowTile);
-              const uint32_t acc = (ks > 0 || j > 0) ? 1u : 0u;
-              if (ACT == 0)
-                tc_mma_pair_mxf8f6f4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
-                                     sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
-              else
-                tc_mma_pair_mxf4(tmem_base, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc,
-                                 sf_col + (kblk >> 2) * 4, sf_col + kSfaCols + (kblk >> 2) * kSfbCols, acc);
-            }
+            tc_commit_pair_mc(empty_a(sa), 0x3);
+            tc_commit_pair_mc(empty_w(sw), 0x3);
           }
-          if (el) tc_commit_pair_mc(empty_bar(slot), 0x3);
           __syncwarp();
+          (void)kSfbCols;
           issued = true;
-          if (++slot == kPStages) {
-            slot = 0;
-            phase ^= 1u;
+          if (++sa == kPStagesA) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sw == kPStagesW) {
+            sw = 0;
+            pw ^= 1u;
           }
         }
         if (!ok) break;
@@ -863,9 +851,9 @@ cudaError_t launch_tail_wide_typed(const GemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t s) {
-  if (!a.w_sf_tiled) return cudaErrorInvalidValue;  // pairs stage prepacked weight scales only
-  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_pair_typed<0, 0>(a, s) : launch_pair_typed<0, 1>(a, s);
-  return a.epilogue == 0 ? launch_pair_typed<1, 0>(a, s) : launch_pair_typed<1, 1>(a, s);
+  // A8W4, prepacked weight scales, K a multiple of 128
+  if (!a.w_sf_tiled || a.act_fmt != 0 || a.K % 128 != 0) return cudaErrorInvalidValue;
+  return a.epilogue == 0 ? launch_pair_typed<0, 0>(a, s) : launch_pair_typed<0, 1>(a, s);
 }
 
 cudaError_t launch_gemm_tail_wide(const GemmArgs& a, cudaStream_t s) {

@@ -64,10 +64,11 @@ def test_expired_wait_is_reported_and_the_context_survives(schedule):
     assert words[1] == 1                 # an expiry was recorded
     # the first expiry: stage 0's full barrier in the MMA warp (index 0, warp 1) or the
     # accumulator-ready barrier in an epilogue warp (index 2 * stages = 12: the chain and fused
-    # schedules run a 6-stage ring for 16-row slots, the CTA-pair kernel a 6-stage ring), warps
-    # 2-9, or -- fused schedule -- the combine's wait for every GEMM2 part in a CTA with no work of
-    # its own (1000 + its sync word offset 1), whichever came first
-    acc_ready = 12
+    # schedules run a 6-stage ring for 16-row slots; 2 * (5 + 8) = 26 in the CTA-pair kernel of a
+    # split GEMM, which runs a 5-stage activation ring and an 8-stage weight ring), warps 2-9, or
+    # -- fused schedule -- the combine's wait for every GEMM2 part in a CTA with no work of its own
+    # (1000 + its sync word offset 1), whichever came first
+    acc_ready = 26 if schedule.startswith("split") else 12
     ok = (words[2], words[5]) == (0, 1) or (words[2] == acc_ready and 2 <= words[5] <= 9)
     if schedule == "fused":
         ok = ok or (words[2] == 1001 and 2 <= words[5] <= 9)
