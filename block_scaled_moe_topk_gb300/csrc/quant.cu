@@ -24,18 +24,20 @@ constexpr int kQuantThreads = 256;
 // Thread i of the grid owns elements [16c, 16c + 16) of row r, (r, c) = (i / (K/16), i % (K/16));
 // lanes 2m and 2m+1 hold one 32-element block (K % 32 == 0 keeps the pairs inside a row) and
 // agree on its amax with one shuffle.  Every lane of a warp runs the same number of rounds.
-template <int FMT>
+// Idx: the flat index type (32 bits whenever rows * K / 16 fits: a 64-bit division per element
+// group is slow).
+template <int FMT, typename Idx>
 __global__ void __launch_bounds__(kQuantThreads) quant_kernel(QuantArgs a) {
   const int K = a.K;
-  const int chunks = K / 16;
-  const int64_t n = a.rows * chunks;
+  const Idx chunks = (Idx)(K / 16);
+  const Idx n = (Idx)a.rows * chunks;
   const int lane = threadIdx.x & 31;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < n; base += stride) {
-    const int64_t i = base + lane;
+  const Idx stride = (Idx)gridDim.x * blockDim.x;
+  for (Idx base = (Idx)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < n; base += stride) {
+    const Idx i = base + lane;
     const bool active = i < n;
-    const int64_t row = active ? i / chunks : 0;
-    const int col0 = active ? (int)(i % chunks) * 16 : 0;
+    const int64_t row = active ? (int64_t)(i / chunks) : 0;
+    const int col0 = active ? (int)(i - (Idx)row * chunks) * 16 : 0;
     float v[16];
     if (active) {
       const uint4* src = reinterpret_cast<const uint4*>(a.x + row * K + col0);
@@ -197,22 +199,25 @@ __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* src,
 }
 
 // Prequantised input: token t's code row (and its scales) copied to its k padded expert rows,
-// scales into the 128x4 tile layout -- the quantiser's scatter without its arithmetic.
+// scales into the 128x4 tile layout -- the quantiser's scatter without its arithmetic.  Idx as
+// for quant_kernel.
+template <typename Idx>
 __global__ void __launch_bounds__(256) permute_rows_kernel(PermuteArgs a) {
   const int64_t row_bytes = a.code_bytes;        // multiple of 16
-  const int64_t chunks = row_bytes / 16;
-  const int64_t n = a.rows * chunks;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / chunks, c = i % chunks;
+  const Idx chunks = (Idx)(row_bytes / 16);
+  const Idx n = (Idx)a.rows * chunks;
+  for (Idx i = (Idx)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (Idx)gridDim.x * blockDim.x) {
+    const int64_t t = (int64_t)(i / chunks);
+    const int64_t c = (int64_t)(i - (Idx)t * chunks);
     const uint4 v = *reinterpret_cast<const uint4*>(a.codes_in + t * row_bytes + c * 16);
     for (int j = 0; j < a.k; ++j)
       *reinterpret_cast<uint4*>(a.codes_out + (int64_t)a.inv_padded[t * a.k + j] * row_bytes + c * 16) = v;
   }
-  const int nb = a.K / 32;
-  const int64_t ns = a.rows * nb;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ns; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / nb;
-    const int kb = (int)(i % nb);
+  const Idx nb = (Idx)(a.K / 32);
+  const Idx ns = (Idx)a.rows * nb;
+  for (Idx i = (Idx)blockIdx.x * blockDim.x + threadIdx.x; i < ns; i += (Idx)gridDim.x * blockDim.x) {
+    const int64_t t = (int64_t)(i / nb);
+    const int kb = (int)(i - (Idx)t * nb);
     const uint8_t v = a.scales_in[t * nb + kb];
     for (int j = 0; j < a.k; ++j) a.scales_out[sf_tile_offset(a.inv_padded[t * a.k + j], kb, a.K)] = v;
   }
@@ -224,7 +229,10 @@ cudaError_t launch_permute_rows(const PermuteArgs& a, cudaStream_t s) {
   const int64_t n = a.rows * (a.code_bytes / 16);
   if (n == 0) return cudaSuccess;
   const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
-  permute_rows_kernel<<<grid, 256, 0, s>>>(a);
+  if (n < ((int64_t)1 << 31))  // rows * K / 32 <= n as well
+    permute_rows_kernel<uint32_t><<<grid, 256, 0, s>>>(a);
+  else
+    permute_rows_kernel<int64_t><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -256,8 +264,14 @@ cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
     return cudaGetLastError();
   }
   const unsigned grid = (unsigned)std::min<int64_t>((n + kQuantThreads - 1) / kQuantThreads, 152 * 8);
-  if (a.fmt == 0) quant_kernel<0><<<grid, kQuantThreads, 0, s>>>(a);
-  else quant_kernel<1><<<grid, kQuantThreads, 0, s>>>(a);
+  const bool narrow = n < ((int64_t)1 << 31);
+  if (a.fmt == 0) {
+    if (narrow) quant_kernel<0, uint32_t><<<grid, kQuantThreads, 0, s>>>(a);
+    else quant_kernel<0, int64_t><<<grid, kQuantThreads, 0, s>>>(a);
+  } else {
+    if (narrow) quant_kernel<1, uint32_t><<<grid, kQuantThreads, 0, s>>>(a);
+    else quant_kernel<1, int64_t><<<grid, kQuantThreads, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
