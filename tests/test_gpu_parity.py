@@ -344,16 +344,24 @@ def _forward_prepacked(x, lg, W, E, k, schedule):
     return out, ws
 
 
+# one split GEMM with the wide tail pass and the other with the single-CTA one: GEMM1 of
+# 2I = 4352 (no multiple of 512) with GEMM2 wide (H = 2048, K = I = 2176: 17 stages), and GEMM1
+# wide (2I = 2048, K = 2048) with GEMM2 of K = 1024 (8 stages)
+_SPLIT_SHAPES = {"mixed_g2_wide": synth.Shape("mixed_g2_wide", 2048, 2176, 8, 2),
+                 "mixed_g1_wide": synth.Shape("mixed_g1_wide", 2048, 1024, 8, 2)}
+
+
 @pytest.mark.parametrize("shape,T,skew", [("tiny", 512, False), ("tiny", 777, True), ("tiny", 2048, True),
                                           ("tiny_wide", 300, False), ("tiny_wide", 512, False),
-                                          ("tiny_wide", 777, True)])
+                                          ("tiny_wide", 777, True), ("mixed_g2_wide", 512, True),
+                                          ("mixed_g1_wide", 512, True)])
 def test_split_gemms_against_oracle_and_single_cta(shape, T, skew):
     """Small shapes with their GEMMs split (skewed routing: experts with 1 to 4+ M tiles, odd
     and even), the whole batch against the oracle and bit for bit against single-CTA tiles.
     tiny_wide (H = I = 2048: N multiples of 512, K of 16 stages) takes the wide tail pass
     (512-column CTA-pair tiles, rotated A-scale atoms), tiny (N = 256) the single-CTA one; at
     T = 300 tiny_wide splits on the wide rule alone (37 rows per expert on average)."""
-    s = synth.SHAPES[shape]
+    s = _SPLIT_SHAPES.get(shape) or synth.SHAPES[shape]
     E, k, H, I = s.E, s.k, s.H, s.I
     assert moe.moe_forward_split_gemms(T, H, I, E, k, moe.MOE_ACT_MXFP8, moe.MOE_SCHEDULE_AUTO, True) == 3
     W = Weights(E, H, I, seed=0, device=DEV, from_bf16=True)
