@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_decode_kernel(const __grid_c
     scatter_pairs(lane);
     named_barrier(1, 32 + 32 * kDEpiWarps);
     // converged loop, one elected lane issues the copies; lane 0 alone polls the global
-    // counters and passes the verdict on (a warp barrier orders its acquire before the copies)
+    // counters and passes the result on (a warp barrier orders its acquire before the copies)
     {
       int slot = 0;
       uint32_t phase = 0;
