@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
 // the routing kernel + scan_cols_kernel + scatter_kernel.
 constexpr int kSmallMaxRows = kSmallRouteTokens * kMaxTopK;
 
-template <int kPerLane>
+template <int kPerLane, int kV>
 __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArgs ra, SortArgs sa) {
   __shared__ int cnt[kMaxExperts];
   __shared__ int next[kMaxExperts];
@@ -155,15 +155,33 @@ __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArg
     next[e] = 0;
   }
   __syncthreads();
-  for (int64_t t = warp; t < T; t += kScanThreads / 32) {
-    int id;
-    float w;
-    route_token_fast<kPerLane>(ra.logits + t * E, E, k, lane, id, w);
-    if (lane < k) {
-      ra.ids[t * k + lane] = id;
-      ra.w[t * k + lane] = w;
-      ids_s[t * k + lane] = id;
-      atomicAdd(&cnt[id], 1);
+  if (kV > 0) {
+    // eight lanes per token, four tokens per warp: the whole batch in one round
+    const int g = lane & 7;
+    for (int64_t t0 = (int64_t)warp * 4; t0 < T; t0 += (kScanThreads / 32) * 4) {
+      const int64_t t = t0 + (lane >> 3);
+      const bool valid = t < T;
+      int id;
+      float w;
+      route_token8<(kV > 0 ? kV : 8)>(ra.logits + (valid ? t : 0) * E, valid, E, k, g, id, w);
+      if (valid && g < k) {
+        ra.ids[t * k + g] = id;
+        ra.w[t * k + g] = w;
+        ids_s[t * k + g] = id;
+        atomicAdd(&cnt[id], 1);
+      }
+    }
+  } else {
+    for (int64_t t = warp; t < T; t += kScanThreads / 32) {
+      int id;
+      float w;
+      route_token_fast<kPerLane>(ra.logits + t * E, E, k, lane, id, w);
+      if (lane < k) {
+        ra.ids[t * k + lane] = id;
+        ra.w[t * k + lane] = w;
+        ids_s[t * k + lane] = id;
+        atomicAdd(&cnt[id], 1);
+      }
     }
   }
   __syncthreads();
@@ -228,8 +246,13 @@ __global__ void __launch_bounds__(kScanThreads) route_sort_small_kernel(RouteArg
 
 cudaError_t launch_route_sort_small(const RouteArgs& ra, const SortArgs& sa, cudaStream_t s) {
   if (ra.T == 0) return cudaSuccess;
-  if (ra.E <= 512) route_sort_small_kernel<16><<<1, kScanThreads, 0, s>>>(ra, sa);
-  else route_sort_small_kernel<32><<<1, kScanThreads, 0, s>>>(ra, sa);
+  // E <= 128: eight lanes per token (16 logits a lane), the batch in one round; more experts
+  // made each token's rounds too long (E = 384: 17-25 -> 35-42 us at T = 8-64), so 32 lanes a
+  // token and the warps take the tokens in turn
+  if (ra.E <= 64) route_sort_small_kernel<16, 8><<<1, kScanThreads, 0, s>>>(ra, sa);
+  else if (ra.E <= 128) route_sort_small_kernel<16, 16><<<1, kScanThreads, 0, s>>>(ra, sa);
+  else if (ra.E <= 512) route_sort_small_kernel<16, 0><<<1, kScanThreads, 0, s>>>(ra, sa);
+  else route_sort_small_kernel<32, 0><<<1, kScanThreads, 0, s>>>(ra, sa);
   return cudaGetLastError();
 }
 
