@@ -48,34 +48,47 @@ namespace {
 // loaded latency), and a CTA's activation tile (16 KiB a stage, mostly L2 hits: the expert's
 // other N tiles read it too) would otherwise take as many slots.
 constexpr int kPStagesA = 5;                       // activation ring
-constexpr int kPStagesW = 8;                       // weight ring: 8 x 8 KiB of weights in flight
 constexpr int kPThreads = 352;
 constexpr int kPEpiWarps = 8;
 constexpr int kPBWarp = 10;
 constexpr int kPHalfRows = 128;                    // weight rows per CTA (half of kNTile)
 constexpr int kPABytes = kRowTile * 128;           // 128 activation rows x 128 bytes
 constexpr int kPBBytes = kPHalfRows * 128;         // 128 weight rows x 128 bytes (smem footprint)
-constexpr int kPWOff = kPStagesA * kPABytes;       // the weight ring after the activation ring
-constexpr int kPSfaOff = kPWOff + kPStagesW * kPBBytes;   // activation-scale atoms, 512 B a slot
-constexpr int kPSfbOff = kPSfaOff + kPStagesA * 512;      // weight-scale atoms, 2 x 512 B a slot
-constexpr int kPBarOff = kPSfbOff + kPStagesW * 1024;
-constexpr int kPBaseOff = kPBarOff + 256;          // pair-tile prefix over experts, int32 [E+1]
-constexpr int kPSmemBytes = kPBaseOff + 4 * (kMaxExperts + 1) + 1024;
+constexpr int kPOutStageBytes = 32 * 32 * 2;       // GEMM2 epilogue staging: 32 rows x 32 bf16 per warp
 constexpr uint32_t kPTmemCols = 512;
 constexpr uint32_t kPSfCol0 = 256;                 // accumulator: columns [0, 256)
 constexpr uint32_t kPSfSlotCols = 12;              // 4 A-scale + 8 weight-scale columns
-static_assert(kPSmemBytes <= 232448, "pair GEMM shared memory");
-static_assert(kPWOff % 1024 == 0 && kPSfaOff % 1024 == 0, "pair GEMM ring alignment");
-static_assert(8 * (2 * kPStagesA + 2 * kPStagesW + 3) + 8 <= 256, "pair GEMM barriers");
 // TMEM scale slots follow the activation ring: the copy for stage i + kPStagesA is issued only
 // after the activation slot of stage i was released, i.e. after stage i's MMAs completed.
 static_assert(kPSfCol0 + kPStagesA * kPSfSlotCols <= kPTmemCols, "pair GEMM TMEM scale slots");
+
+// Shared memory: the activation ring, the weight ring (8 x 8 KiB of weights in flight; 7 for
+// GEMM2, whose rows leave through a per-warp staging buffer as TMA stores -- direct 16-byte stores
+// from every lane cost GEMM2's pairs ~5 % in competition with the weight stream), the scale
+// atoms of both rings, the staging buffers, the barriers and the pair-tile prefix.
+template <int EPI>
+struct PairGeo {
+  static constexpr bool kOutStaging = EPI == 1;
+  static constexpr int kStagesW = kOutStaging ? 7 : 8;
+  static constexpr int kWOff = kPStagesA * kPABytes;              // the weight ring after the activation ring
+  static constexpr int kSfaOff = kWOff + kStagesW * kPBBytes;     // activation-scale atoms, 512 B a slot
+  static constexpr int kSfbOff = kSfaOff + kPStagesA * 512;       // weight-scale atoms, 2 x 512 B a slot
+  static constexpr int kOutOff = (kSfbOff + kStagesW * 1024 + 1023) / 1024 * 1024;
+  static constexpr int kOutBytes = kOutStaging ? kPEpiWarps * kPOutStageBytes : 0;
+  static constexpr int kBarOff = kOutStaging ? kOutOff + kOutBytes : kSfbOff + kStagesW * 1024;
+  static constexpr int kBaseOff = kBarOff + 256;                  // pair-tile prefix over experts, int32 [E+1]
+  static constexpr int kSmemBytes = kBaseOff + 4 * (kMaxExperts + 1) + 1024;
+  static_assert(kSmemBytes <= 232448, "pair GEMM shared memory");
+  static_assert(kWOff % 1024 == 0 && kSfaOff % 1024 == 0, "pair GEMM ring alignment");
+  static_assert(8 * (2 * kPStagesA + 2 * kStagesW + 3) + 8 <= 256, "pair GEMM barriers");
+};
 
 struct PairParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_act;  // activation codes [rows_cap, K or K/2], box 128 B x 128 rows
   CUtensorMap tmap_w;    // weights [E, N, K/2], box 128 K x 128 rows x 1
   CUtensorMap tmap_asf;  // activation scales as rows of 256 bytes, box 256 x (2 * atoms per stage)
   CUtensorMap tmap_wsf;  // prepacked weight scales as rows of 256 bytes, same box
+  CUtensorMap tmap_out;  // GEMM2: y2 bf16 [rows_cap, N], box 32 columns x 32 rows, 64-byte swizzle
   const int32_t* counts;
   const int32_t* mtile_base;  // expert e's rows start at row 128 * mtile_base[e]
   const uint8_t* act_sf;      // activation scales, 128x4 tile layout
@@ -122,6 +135,10 @@ template <int ACT, int EPI>
 __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __grid_constant__ PairParams p) {
   static_assert(ACT == 0, "the pair kernel serves A8W4 (E4M3 x E2M1)");
   using TR = ActTraits<ACT>;
+  using G = PairGeo<EPI>;
+  constexpr int kPStagesW = G::kStagesW;
+  constexpr int kPWOff = G::kWOff, kPSfaOff = G::kSfaOff, kPSfbOff = G::kSfbOff, kPBarOff = G::kBarOff,
+                kPBaseOff = G::kBaseOff;
   constexpr int kMmaPerStage = TR::kKPerStage / TR::kMmaK;  // 4
   constexpr uint32_t kSfaCols = 4;
   constexpr uint32_t kScaleBoxBytes = 512;                  // one k-atom a stage
@@ -379,8 +396,39 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);  // registers hold the tile
       acc_phase ^= 1u;
-      store_acc_rows<ACT, EPI>(acc, valid, prow, pt.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16);
+      if (G::kOutStaging && __all_sync(0xffffffffu, valid)) {
+        // GEMM2 rows as bf16 (nearest even) through shared memory when all 32 rows of this warp
+        // are routed rows: each 32-column chunk leaves as one TMA store (as in gemm.cu)
+        const uint32_t buf = sbase + G::kOutOff + (uint32_t)(warp - 2) * kPOutStageBytes;
+        const int x0 = pt.nt * kNTile + half * 128;
+        const int y0 = (int)(prow - lane);
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-byte swizzle: 16-byte chunk ^= (row/2)%4
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (lane == 0) bulk_wait_read_all();  // the previous store has read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(acc[32 * c + 8 * i + 2 * q], acc[32 * c + 8 * i + 2 * q + 1]);
+              w[q] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            st_shared_v4(buf + (uint32_t)lane * 64u + (((uint32_t)i ^ swz) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmap_out, buf, x0 + 32 * c, y0);
+            bulk_commit_group();
+          }
+        }
+      } else {
+        store_acc_rows<ACT, EPI>(acc, valid, prow, pt.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16);
+      }
     }
+    if (G::kOutStaging && lane == 0) bulk_wait_all();  // this warp's y2 stores have completed
   }
 
   tc_fence_before();
@@ -424,13 +472,13 @@ cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.dynamicSmemBytes = PairGeo<EPI>::kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_clusters[dev].load(std::memory_order_acquire) == 0) {
     err = cudaFuncSetAttribute(moe_gemm_pair_kernel<ACT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kPSmemBytes);
+                               PairGeo<EPI>::kSmemBytes);
     if (err != cudaSuccess) return err;
     int n = 0;
     cfg.gridDim = dim3(2 * a.num_sms / 2);
@@ -481,6 +529,16 @@ cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
   if (encode_scale_rows(encode, &p.tmap_asf, a.act_sf, asf_bytes, atoms) != CUDA_SUCCESS ||
       encode_scale_rows(encode, &p.tmap_wsf, a.w_sf, wsf_bytes, atoms) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  if (EPI == 1) {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.rows_cap};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.N * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&p.tmap_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_bf16, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   p.counts = a.counts;
   p.mtile_base = a.mtile_base;
   p.act_sf = a.act_sf;
