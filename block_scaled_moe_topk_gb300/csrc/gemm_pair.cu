@@ -1,11 +1,12 @@
-// gemm_pair.cu -- the grouped block-scaled GEMMs of the expert layer on CTA pairs, for the
-// experts' whole pairs of M tiles (A8W4 or A4W4, weight scales in the 128x4 tile layout).
+// gemm_pair.cu -- the grouped block-scaled GEMMs of the expert layer on CTA pairs (A8W4, weight
+// scales in the 128x4 tile layout): the pair kernel over the experts' whole pairs of M tiles, and
+// the wide tail pass over their odd last M tiles (further below).
 //
 // Same contract as gemm.cu (GEMM1: SwiGLU + MX requant epilogue over the gate/up-interleaved
 // W1 rows, "feat(moe): FlyDSL MegaMoE fused EP-MoE integration", description: INTERLEAVE(g1u1);
-// GEMM2: bf16 rows).  An expert with m M tiles has m / 2 (rounded down) pair tiles here; its
-// odd last M tile, if any, is left to gemm.cu's tail pass (GemmArgs::tail_only), which runs
-// right after this kernel on the same stream.
+// GEMM2: bf16 rows).  An expert with m M tiles has m / 2 (rounded down) pair tiles in the pair
+// kernel; its odd last M tile, if any, is left to the wide tail pass or to gemm.cu's tail pass
+// (GemmArgs::tail_only), which runs right after the pair kernel on the same stream.
 //
 // A pair tile is 256 routed rows -- two consecutive 128-row M tiles of one expert -- by 256
 // output columns, computed by a cluster of two CTAs on two SMs with tcgen05.mma.cta_group::2
@@ -24,8 +25,8 @@
 //     the MMA commits release the stage's slots in both CTAs (multicast), and the accumulator
 //     hand-off goes to both epilogues, whose "TMEM free" arrivals go back to the even CTA.
 // Measured (V4-Pro A8W4, T = 8192): a pair stage costs ~0.32 us per SM against ~0.42 for the
-// single kernel's, so the pairs plus the tail pass run GEMM1 in 1.94 ms against 2.13 ms for
-// single-CTA tiles throughout.
+// single kernel's; the pairs plus the single-CTA tail pass ran GEMM1 in 1.94 ms against 2.13 ms
+// for single-CTA tiles throughout, and with the wide tail pass in ~1.86 ms.
 // Warp roles per CTA: 0 activation-side TMA, 10 weight-side TMA (both converged, copies issued
 // by an elected lane), 1 TMEM (+ MMA issue in the even CTA), 2..9 epilogue (as in gemm.cu).
 // Every wait is bounded; on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT, lets its copies and
