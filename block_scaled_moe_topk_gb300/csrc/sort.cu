@@ -65,8 +65,12 @@ __global__ void __launch_bounds__(kColWarps * 32) scan_cols_kernel(SortArgs a) {
 // of the routed rows and of the 128-row padded rows from counts[] (every chunk's warp does
 // this for itself; chunk 0's also writes offsets, padded offsets and M-tile bases), then walks
 // its pairs in order and places each at offset[e] + chunk_base[e] + rank, so equal experts
-// keep pair order.  Dynamic shared memory: E x (int64 offset, int64 padded offset, int32 next).
+// keep pair order.  Every global load (the expert totals, this chunk's column of the per-chunk
+// histogram, the chunk's expert ids) is issued before the first is used, so the warp pays one
+// load latency instead of one per phase and per pass.  Dynamic shared memory: E x (int64 offset,
+// int64 padded offset, int32 next).
 __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
+  static_assert(kTokensPerChunk == 32, "one pass of the warp per slot");
   extern __shared__ __align__(8) uint8_t sort_smem[];
   const int lane = threadIdx.x;
   const int E = a.E, k = a.k;
@@ -74,7 +78,26 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
   int64_t* poff_s = off_s + E;
   int* next = reinterpret_cast<int*>(poff_s + E);
   const int64_t b = blockIdx.x;
-  for (int e = lane; e < E; e += 32) next[e] = a.counts[e];
+  constexpr int kPer = kMaxExperts / 32;
+  int cnt[kPer], col[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    cnt[i] = e < E ? a.counts[e] : 0;
+    col[i] = e < E ? a.chunk_hist[(int64_t)e * a.nchunk + b] : 0;
+  }
+  const int64_t q_begin = b * kTokensPerChunk * k;
+  const int64_t q_lim = q_begin + (int64_t)kTokensPerChunk * k;
+  const int64_t q_end = (a.T * k < q_lim) ? a.T * k : q_lim;
+  int idv[kMaxTopK];  // pass j holds pairs q_begin + 32 j + lane
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    const int64_t q = q_begin + 32 * j + lane;
+    idv[j] = (j < k && q < q_end) ? a.ids[q] : -1;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (lane + 32 * i < E) next[lane + 32 * i] = cnt[i];
   __syncwarp();
   // lane L owns experts [L * per, L * per + per)
   const int per = (E + 31) / 32;
@@ -106,16 +129,17 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a) {
     if (a.mtile_base) a.mtile_base[E] = (int32_t)(xsp / kRowTile);
   }
   __syncwarp();
-  for (int e = lane; e < E; e += 32) next[e] = a.chunk_hist[(int64_t)e * a.nchunk + b];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (lane + 32 * i < E) next[lane + 32 * i] = col[i];
   __syncwarp();
-  const int64_t q_begin = b * kTokensPerChunk * k;
-  const int64_t q_lim = q_begin + (int64_t)kTokensPerChunk * k;
-  const int64_t q_end = (a.T * k < q_lim) ? a.T * k : q_lim;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int64_t q0 = q_begin; q0 < q_end; q0 += 32) {
-    const int64_t q = q0 + lane;
-    int id = (q < q_end) ? a.ids[q] : -1;
-    const bool valid = id >= 0 && id < E;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j >= k) break;
+    const int64_t q = q_begin + 32 * j + lane;
+    int id = idv[j];
+    const bool valid = q < q_end && id >= 0 && id < E;
     if (!valid) id = -1 - lane;  // a group of its own
     const uint32_t peers = __match_any_sync(0xffffffffu, id);
     const int rank = __popc(peers & lt_mask);
