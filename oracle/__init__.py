@@ -191,12 +191,17 @@ def f64_to_bf16(v: float) -> int:
 
 
 def moe_forward(x_bits, logits, w1, w1s, w2, w2s, E: int, k: int, act_fmt: int, tokens=None,
-                diagnostics: bool = False, nthreads: int | None = None, h_bf16: bool = False):
+                diagnostics: bool = False, nthreads: int | None = None, h_bf16: bool = False,
+                y2_fp8: bool = False):
     """The whole expert layer for the listed tokens (all tokens if None).
 
     h_bf16: round the SwiGLU output h to bf16 before its MX quantisation (the bf16-out stage-1
     form of "[HIP] gfx950 A8W4 fused_moe configs for DSv4.1 TP-sharded experts", How the rows
     were chosen); by default h is quantised from fp32, as the fused stage-1 epilogue does.
+    y2_fp8: the weighted GEMM2 rows w_j * y2 (fp32 product) travel as E4M3 codes with one E8M0
+    scale per 1x32 block and the combine sums their dequantised values (the FP8 transport of the
+    stage-2 rows in "add A4W4 and FP8 P2P transport support to MegaMoE", Technical Details);
+    by default the fp32 rows are weighted and summed directly.
 
     x_bits uint16 [T, H] (bf16 bit patterns), logits fp32 [T, E],
     w1 uint8 [E, 2I, H/2], w1s uint8 [E, 2I, H/32], w2 uint8 [E, H, I/2], w2s uint8 [E, H, I/32].
@@ -231,7 +236,7 @@ def moe_forward(x_bits, logits, w1, w1s, w2, w2s, E: int, k: int, act_fmt: int, 
         _ptr(tok), n, _ptr(out),
         _ptr(diag["h"]) if diag else None, _ptr(diag["a2"]) if diag else None,
         _ptr(diag["a2s"]) if diag else None, _ptr(diag["y2"]) if diag else None, int(nthreads),
-        1 if h_bf16 else 0)
+        (1 if h_bf16 else 0) | (2 if y2_fp8 else 0))
     if rc != 0:
         raise ValueError("oracle_moe_forward rejected its arguments")
     return (out, diag) if diagnostics else out

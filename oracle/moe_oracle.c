@@ -346,6 +346,9 @@ static float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
  * Returns 0, or -1 on bad arguments.
  */
 #define ORACLE_OPT_H_BF16 1 /* round h to bf16 (nearest even) before its MX quantisation */
+#define ORACLE_OPT_Y2_FP8 2 /* the weighted GEMM2 rows w_j * y2 (fp32 product) quantised to E4M3
+                             with one E8M0 scale per 1x32 block, the combine summing their
+                             dequantised values (FP8 transport of the stage-2 rows) */
 
 static float round_bf16(float v) {
   const uint32_t bits = (uint32_t)f64_to_bf16_rne((double)v) << 16;
@@ -388,6 +391,9 @@ int oracle_moe_forward_opts(const uint16_t* x, const float* logits, const uint8_
     uint8_t* a2 = (uint8_t*)malloc((size_t)a2_row);
     uint8_t* a2s = (uint8_t*)malloc((size_t)(I / 32));
     double* a2d = (double*)malloc(sizeof(double) * (size_t)I);
+    float* yw = (float*)malloc(sizeof(float) * (size_t)H); /* weighted row, FP8 transport */
+    uint8_t* yq = (uint8_t*)malloc((size_t)H);
+    uint8_t* ys = (uint8_t*)malloc((size_t)(H / 32));
 
     for (int j = 0; j < k; ++j) {
       int e = ids[j];
@@ -416,14 +422,19 @@ int oracle_moe_forward_opts(const uint16_t* x, const float* logits, const uint8_
         for (int c = 0; c < I; ++c) s += a2d[c] * dequant_elem(wr, ws, c, ORACLE_FMT_E2M1);
         float y = (float)s;
         if (y2_out) y2_out[(it * k + j) * (int64_t)H + n] = y;
-        acc[n] += (double)w[j] * (double)y;
+        if (opts & ORACLE_OPT_Y2_FP8) yw[n] = w[j] * y;
+        else acc[n] += (double)w[j] * (double)y;
+      }
+      if (opts & ORACLE_OPT_Y2_FP8) {
+        oracle_quantize_rows_f32(yw, 1, H, ORACLE_FMT_E4M3, yq, ys);
+        for (int n = 0; n < H; ++n) acc[n] += dequant_elem(yq, ys, n, ORACLE_FMT_E4M3);
       }
       if (h_out) memcpy(h_out + (it * k + j) * (int64_t)I, h, sizeof(float) * (size_t)I);
       if (a2_codes) memcpy(a2_codes + (it * k + j) * a2_row, a2, (size_t)a2_row);
       if (a2_scales) memcpy(a2_scales + (it * k + j) * (int64_t)(I / 32), a2s, (size_t)(I / 32));
     }
     for (int n = 0; n < H; ++n) out[it * (int64_t)H + n] = f64_to_bf16_rne(acc[n]);
-    free(xq); free(xs); free(xd); free(acc); free(h); free(a2); free(a2s); free(a2d);
+    free(xq); free(xs); free(xd); free(acc); free(h); free(a2); free(a2s); free(a2d); free(yw); free(yq); free(ys);
   }
   return 0;
 }

@@ -294,10 +294,12 @@ def _tiny_case(T=16, H=256, I=128, E=8, k=2, seed=0, act=E4M3):
                 w1b=w1b, w2b=w2b)
 
 
-def _dense_masked(c, h_bf16=False):
+def _dense_masked(c, h_bf16=False, y2_fp8=False):
     """Brute force over ALL experts for every token, masked by the routing:
     no sort, no gather, numpy matmuls, the numpy MX restatement, torch softmax.
-    h_bf16: h rounded to bf16 (numpy round-to-nearest-even) before its quantisation."""
+    h_bf16: h rounded to bf16 (numpy round-to-nearest-even) before its quantisation.
+    y2_fp8: each expert's rows weighted in fp32 (the routing weights, pinned above) and
+    passed through the numpy E4M3 restatement before they are summed."""
     T, H, I, E, k, act = c["T"], c["H"], c["I"], c["E"], c["k"], c["act"]
     x = mx_ref.bf16_bits_to_f64(c["x"]).astype(np.float32)
     xq, _ = mx_ref.quantize_values(x, act)
@@ -309,6 +311,11 @@ def _dense_masked(c, h_bf16=False):
     for t in range(T):
         top = sorted(range(E), key=lambda e: (-float(c["lg"][t, e]), e))[:k]
         mask[t, top] = p[t, top] / p[t, top].sum()
+    wmask = np.zeros((T, E), np.float32)  # the fp32 routing weights the layer applies
+    if y2_fp8:
+        ids, w = oracle.route(c["lg"], k)
+        for t in range(T):
+            wmask[t, ids[t]] = w[t]
     out = np.zeros((T, H))
     for e in range(E):
         acc = (xq @ W1[e].T).astype(np.float32)  # [T, 2I]
@@ -318,7 +325,12 @@ def _dense_masked(c, h_bf16=False):
             h = mx_ref.bf16_rne(h.astype(np.float64)).astype(np.float32)
         a2, _ = mx_ref.quantize_values(h, act)
         y2 = (a2 @ W2[e].T).astype(np.float32).astype(np.float64)
-        out += mask[:, e:e + 1].astype(np.float32).astype(np.float64) * y2
+        if y2_fp8:
+            v = wmask[:, e:e + 1] * y2.astype(np.float32)  # fp32 product
+            q, _ = mx_ref.quantize_values(v, E4M3)
+            out += q
+        else:
+            out += mask[:, e:e + 1].astype(np.float32).astype(np.float64) * y2
     return out
 
 
@@ -331,6 +343,23 @@ def test_forward_equals_dense_masked_brute_force(act, h_bf16):
     want = _dense_masked(c, h_bf16)
     ulp = np.ldexp(1.0, np.frexp(np.abs(want) + 1e-30)[1] - 8)
     assert np.all(np.abs(got - want) <= ulp), np.abs(got - want).max()
+
+
+@pytest.mark.parametrize("act", [E4M3, E2M1])
+def test_y2_fp8_option_equals_dense_masked_brute_force(act):
+    """FP8 transport of the stage-2 rows ("add A4W4 and FP8 P2P transport support to MegaMoE",
+    Technical Details): the weighted rows quantised to E4M3 with one E8M0 scale per 1x32 block
+    before the combine.  The brute force builds it from the numpy MX restatement and the pinned
+    routing weights; the option moves the output by E4M3 rounding (a few percent), no more."""
+    c = _tiny_case(act=act)
+    args = (c["x"], c["lg"], c["w1"], c["w1s"], c["w2"], c["w2s"], c["E"], c["k"], act)
+    got = mx_ref.bf16_bits_to_f64(oracle.moe_forward(*args, y2_fp8=True))
+    want = _dense_masked(c, y2_fp8=True)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(want) + 1e-30)[1] - 8)
+    assert np.all(np.abs(got - want) <= ulp), np.abs(got - want).max()
+    base = mx_ref.bf16_bits_to_f64(oracle.moe_forward(*args))
+    rel = np.linalg.norm(got - base) / np.linalg.norm(base)
+    assert 1e-3 < rel < 0.1, rel
 
 
 @pytest.mark.parametrize("act", [E4M3, E2M1])
