@@ -286,6 +286,13 @@ def run_ours(args):
     g_c = graph_for(x, lg, out, f=moe.moe_a8w4_forward, weights=Wc)
     canon_ms = statistics.median(timed_replays(g_c, max(5, min(args.steps, 20)), 3))
     del g_c
+    # the same call with the GEMM2 rows in FP8 transport form (MOE_SCHEDULE_CHAIN_FP8_Y2)
+    def fwd_fp8(x_, lg_, *rest, stream=None):
+        return moe.moe_forward_ex(x_, lg_, *rest, weight_scales_prepacked=True,
+                                  schedule=moe.MOE_SCHEDULE_CHAIN_FP8_Y2, stream=stream)
+    g_f = graph_for(x, lg, out, f=fwd_fp8)
+    fp8_ms = statistics.median(timed_replays(g_f, max(5, min(args.steps, 20)), 3))
+    del g_f
     ms_per_step = total_ms / args.steps
     value = job_throughput(world, T, args.steps, total_ms)
 
@@ -484,6 +491,7 @@ def run_ours(args):
                     "p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2)},
         "canonical_scales_us_per_call": round(canon_ms * 1e3, 2),
         "prequant_us_per_call": round(pre_ms * 1e3, 2),
+        "fp8_y2_us_per_call": round(fp8_ms * 1e3, 2),
         "a4w4": a4, "config_sweeps": cfg,
         "layer_roofline": {"bytes": B, "flops": F, "active_experts": active, "t_hbm_us": round(th * 1e6, 2),
                            "t_tensor_us": round(tt * 1e6, 2), "bound": "hbm" if th >= tt else "tensor",

@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "MoeError", "MOE_ACT_MXFP8", "MOE_ACT_MXFP4", "MOE_SCHEDULE_AUTO", "MOE_SCHEDULE_CHAIN", "MOE_SCHEDULE_FUSED",
-    "MOE_SCHEDULE_CHAIN_BF16_H", "MOE_SCHEDULE_CHAIN_SINGLE_CTA", "lib", "moe_status_string", "moe_workspace_bytes",
+    "MOE_SCHEDULE_CHAIN_BF16_H", "MOE_SCHEDULE_CHAIN_SINGLE_CTA", "MOE_SCHEDULE_CHAIN_FP8_Y2", "lib", "moe_status_string", "moe_workspace_bytes",
     "moe_get_workspace_layout", "moe_topk_route", "moe_sort_by_expert", "moe_sort_by_expert_noalloc",
     "moe_quantize_mx", "moe_a8w4_forward",
     "moe_a4w4_forward", "moe_forward_ex", "moe_a8w4_forward_prequant", "moe_a4w4_forward_prequant", "moe_prepack_scales", "moe_a8w4_forward_prepacked", "moe_a4w4_forward_prepacked",
@@ -31,6 +31,7 @@ MOE_SCHEDULE_CHAIN = 1  # kernel chain, one CTA per 128 x 256 GEMM tile over the
 MOE_SCHEDULE_FUSED = 2  # T <= 64: the whole layer in one persistent kernel
 MOE_SCHEDULE_CHAIN_BF16_H = 3  # kernel chain, GEMM1 writes bf16 h, a separate kernel requantises
 MOE_SCHEDULE_CHAIN_SINGLE_CTA = 4  # kernel chain with single-CTA GEMM tiles only (no pair split)
+MOE_SCHEDULE_CHAIN_FP8_Y2 = 5  # kernel chain, GEMM2 rows travel as weighted E4M3 + E8M0 scales
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_topk.so")
 
 STATUS_NAMES = {

@@ -1,6 +1,6 @@
 // gemm.cu -- grouped block-scaled GEMMs of the expert layer on the tcgen05 tensor cores.
 //
-// One persistent kernel, two epilogues:
+// One persistent kernel; its epilogues:
 //   GEMM1 (EPI=0): acc[r, n] = sum_K xq[r, K] * W1[e, n, K], n in [0, 2I) with rows 2j = gate_j,
 //                  2j+1 = up_j ("feat(moe): FlyDSL MegaMoE fused EP-MoE integration", description:
 //                  INTERLEAVE(g1u1)); the epilogue forms h_j = silu(gate_j) * up_j and requantises
@@ -8,6 +8,9 @@
 //                  for A4W4 ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical
 //                  Details) and as E4M3 codes for A8W4.
 //   GEMM2 (EPI=1): y2[r, n] = sum_I a2[r, I] * W2[e, n, I], accumulated in fp32, stored as bf16.
+//   GEMM2 (EPI=3, FP8 transport): the same rows times their routing weights, stored as E4M3
+//                  codes with one E8M0 scale per 1x32 block (same page, Technical Details).
+//   GEMM1 (EPI=2, bf16-out form): h as bf16 rows for a separate requantisation kernel.
 //
 // Tiles are 128 routed rows (one expert's padded segment) x 256 output columns.  Per CTA:
 //   warp 0      producer: TMA (activation tile 128x128B, weight tile 256x128B) and a bulk copy
@@ -95,6 +98,7 @@ struct GemmParams {  // 64-byte aligned through its CUtensorMap members
   uint8_t* out_codes;
   uint8_t* out_sf;
   uint16_t* out_bf16;
+  const float* row_w;     // epilogue 3: routing weight of each padded row
   uint32_t* status;
   uint64_t timeout_ns;
   int E, N, K;
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           }
         }
       } else {
-        store_acc_rows<ACT, EPI>(acc, valid, prow, tc.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16);
+        store_acc_rows<ACT, EPI>(acc, valid, prow, tc.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16, p.row_w);
       }
     }
   }
@@ -478,6 +482,7 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   p.out_codes = a.out_codes;
   p.out_sf = a.out_sf;
   p.out_bf16 = a.out_bf16;
+  p.row_w = a.row_w;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   p.E = a.E;
@@ -490,24 +495,25 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// a_rows = 16: no tile has more routed rows; 64: 64-row work units (any routing); else 128.
+// A4W4's larger stages gain no extra stage from a 64-row slot.
+template <int EPI>
+cudaError_t launch_epi(const GemmArgs& a, cudaStream_t s) {
+  if (a.a_rows <= 16) return a.act_fmt == 0 ? launch_typed<0, EPI, 16>(a, s) : launch_typed<1, EPI, 16>(a, s);
+  if (a.a_rows <= 64 && a.act_fmt == 0) return launch_typed<0, EPI, 64>(a, s);
+  return a.act_fmt == 0 ? launch_typed<0, EPI, kRowTile>(a, s) : launch_typed<1, EPI, kRowTile>(a, s);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  // a_rows = 16: no tile has more routed rows; 64: 64-row work units (any routing); else 128.
-  // A4W4's larger stages gain no extra stage from a 64-row slot.
-  if (a.epilogue == 2) {  // GEMM1 writing bf16 h (the bf16-out form)
-    if (a.a_rows <= 16) return a.act_fmt == 0 ? launch_typed<0, 2, 16>(a, s) : launch_typed<1, 2, 16>(a, s);
-    if (a.a_rows <= 64 && a.act_fmt == 0) return launch_typed<0, 2, 64>(a, s);
-    return a.act_fmt == 0 ? launch_typed<0, 2, kRowTile>(a, s) : launch_typed<1, 2, kRowTile>(a, s);
+  switch (a.epilogue) {
+    case 0: return launch_epi<0>(a, s);
+    case 1: return launch_epi<1>(a, s);
+    case 2: return launch_epi<2>(a, s);  // GEMM1 writing bf16 h (the bf16-out form)
+    case 3: return launch_epi<3>(a, s);  // GEMM2 rows as weighted FP8 (FP8 transport)
+    default: return cudaErrorInvalidValue;
   }
-  if (a.a_rows <= 16) {
-    if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, 16>(a, s) : launch_typed<0, 1, 16>(a, s);
-    return a.epilogue == 0 ? launch_typed<1, 0, 16>(a, s) : launch_typed<1, 1, 16>(a, s);
-  }
-  if (a.a_rows <= 64 && a.act_fmt == 0)
-    return a.epilogue == 0 ? launch_typed<0, 0, 64>(a, s) : launch_typed<0, 1, 64>(a, s);
-  if (a.act_fmt == 0) return a.epilogue == 0 ? launch_typed<0, 0, kRowTile>(a, s) : launch_typed<0, 1, kRowTile>(a, s);
-  return a.epilogue == 0 ? launch_typed<1, 0, kRowTile>(a, s) : launch_typed<1, 1, kRowTile>(a, s);
 }
 
 }  // namespace moe

@@ -141,9 +141,13 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 //   EPI 1 (GEMM2): the fp32 row rounded to bf16 (nearest even) into out_bf16 [rows, N].
 //   EPI 2 (GEMM1, bf16-out form): h_j = silu(gate_j) * up_j rounded to bf16 into out_bf16
 //                  [rows, N/2], for a separate requantisation kernel.
+//   EPI 3 (GEMM2, FP8 transport): the row times its routing weight row_w[prow] (fp32), four
+//                  32-wide blocks as E4M3 codes into out_codes [rows, N] and one E8M0 byte per
+//                  block into out_sf [rows, N/32] (row-major, for the combine).
 template <int ACT, int EPI>
 __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, int64_t prow, int nt, int half, int N,
-                                               uint8_t* out_codes, uint8_t* out_sf, uint16_t* out_bf16) {
+                                               uint8_t* out_codes, uint8_t* out_sf, uint16_t* out_bf16,
+                                               const float* row_w = nullptr) {
   if (EPI == 0) {
     const int I = N / 2;
     // Padding rows of an expert's segment hold whatever the workspace held before: their
@@ -195,6 +199,26 @@ __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, in
         w[c] = *reinterpret_cast<const uint32_t*>(&hb);
       }
       d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else if (EPI == 3) {
+    if (!valid) return;  // padding rows: nothing stored
+    const float wgt = row_w[prow];
+#pragma unroll
+    for (int i = 0; i < 128; ++i) acc[i] *= wgt;
+    const int c0 = nt * kNTile + half * 128;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      const float* v = acc + 32 * blk;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const MxScale sc = mx_scale<0>(amax);
+      uint4* dst = reinterpret_cast<uint4*>(out_codes + prow * N + c0 + 32 * blk);
+      const uint2 q0 = pack_e4m3x8(v, sc.mult), q1 = pack_e4m3x8(v + 8, sc.mult);
+      const uint2 q2 = pack_e4m3x8(v + 16, sc.mult), q3 = pack_e4m3x8(v + 24, sc.mult);
+      dst[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
+      dst[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
+      out_sf[prow * (N / 32) + c0 / 32 + blk] = sc.byte;
     }
   } else if (valid) {
     uint4* d4 = reinterpret_cast<uint4*>(out_bf16 + prow * N + nt * kNTile + half * 128);

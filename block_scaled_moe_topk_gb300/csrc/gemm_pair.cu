@@ -97,6 +97,7 @@ struct PairParams {  // 64-byte aligned through its CUtensorMap members
   uint8_t* out_codes;
   uint8_t* out_sf;
   uint16_t* out_bf16;
+  const float* row_w;         // epilogue 3: routing weight of each padded row
   uint32_t* status;
   uint64_t timeout_ns;
   int E, N, K;
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
           }
         }
       } else {
-        store_acc_rows<ACT, EPI>(acc, valid, prow, pt.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16);
+        store_acc_rows<ACT, EPI>(acc, valid, prow, pt.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16, p.row_w);
       }
     }
     if (G::kOutStaging && lane == 0) bulk_wait_all();  // this warp's y2 stores have completed
@@ -547,6 +548,7 @@ cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
   p.out_codes = a.out_codes;
   p.out_sf = a.out_sf;
   p.out_bf16 = a.out_bf16;
+  p.row_w = a.row_w;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   p.E = a.E;
@@ -606,6 +608,7 @@ struct TailParams {  // 64-byte aligned through its CUtensorMap members
   uint8_t* out_codes;
   uint8_t* out_sf;
   uint16_t* out_bf16;
+  const float* row_w;         // epilogue 3: routing weight of each padded row
   uint32_t* status;
   uint64_t timeout_ns;
   int E, N, K;
@@ -819,7 +822,7 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_tail_wide_kernel(const 
       if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);  // registers hold the tile
       acc_phase ^= 1u;
       store_acc_rows<ACT, EPI>(acc, valid, prow, 2 * pt.nt + ntl, quad >> 1, p.N, p.out_codes, p.out_sf,
-                               p.out_bf16);
+                               p.out_bf16, p.row_w);
     }
   }
 
@@ -891,6 +894,7 @@ cudaError_t launch_tail_wide_typed(const GemmArgs& a, cudaStream_t s) {
   p.out_codes = a.out_codes;
   p.out_sf = a.out_sf;
   p.out_bf16 = a.out_bf16;
+  p.row_w = a.row_w;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   p.E = a.E;
@@ -912,14 +916,24 @@ cudaError_t launch_tail_wide_typed(const GemmArgs& a, cudaStream_t s) {
 cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t s) {
   // A8W4, prepacked weight scales, K a multiple of 128
   if (!a.w_sf_tiled || a.act_fmt != 0 || a.K % 128 != 0) return cudaErrorInvalidValue;
-  return a.epilogue == 0 ? launch_pair_typed<0, 0>(a, s) : launch_pair_typed<0, 1>(a, s);
+  switch (a.epilogue) {
+    case 0: return launch_pair_typed<0, 0>(a, s);
+    case 1: return launch_pair_typed<0, 1>(a, s);
+    case 3: return launch_pair_typed<0, 3>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_gemm_tail_wide(const GemmArgs& a, cudaStream_t s) {
   // A8W4 with prepacked weight scales, N a multiple of 512, the rotated atoms written
   if (!a.w_sf_tiled || a.act_fmt != 0 || a.N % kTailWideN != 0 || a.K % 128 != 0 || a.act_sf_rot == nullptr)
     return cudaErrorInvalidValue;
-  return a.epilogue == 0 ? launch_tail_wide_typed<0>(a, s) : launch_tail_wide_typed<1>(a, s);
+  switch (a.epilogue) {
+    case 0: return launch_tail_wide_typed<0>(a, s);
+    case 1: return launch_tail_wide_typed<1>(a, s);
+    case 3: return launch_tail_wide_typed<3>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace moe

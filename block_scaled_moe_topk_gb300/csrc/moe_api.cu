@@ -146,7 +146,8 @@ constexpr int kForwardKernels = 7;
 constexpr int kMaxForwardKernels = 9;  // the chain with both GEMMs split (pair kernel + tail pass)
 bool valid_schedule(int schedule) {
   return schedule == MOE_SCHEDULE_AUTO || schedule == MOE_SCHEDULE_CHAIN || schedule == MOE_SCHEDULE_FUSED ||
-         schedule == MOE_SCHEDULE_CHAIN_BF16_H || schedule == MOE_SCHEDULE_CHAIN_SINGLE_CTA;
+         schedule == MOE_SCHEDULE_CHAIN_BF16_H || schedule == MOE_SCHEDULE_CHAIN_SINGLE_CTA ||
+         schedule == MOE_SCHEDULE_CHAIN_FP8_Y2;
 }
 bool use_fused(int64_t T, int schedule, int H, int I) {
   return schedule == MOE_SCHEDULE_FUSED || (schedule == MOE_SCHEDULE_AUTO && moe::decode_auto(T, H, I));
@@ -264,6 +265,12 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
     MOE_CUDA_TRY(mark());
     return MOE_OK;
   }
+  // FP8 transport of the GEMM2 rows: their E4M3 codes [rows_cap, H], E8M0 scales [rows_cap, H/32]
+  // and each padded row's routing weight [rows_cap] share the y2 region (2 H bytes a row)
+  const bool fp8_y2 = schedule == MOE_SCHEDULE_CHAIN_FP8_Y2;
+  uint8_t* y2q = fp8_y2 ? at(L.y2) : nullptr;
+  uint8_t* y2s = fp8_y2 ? y2q + (size_t)L.rows_cap * H : nullptr;
+  float* row_w = fp8_y2 ? reinterpret_cast<float*>(y2s + align256((size_t)L.rows_cap * (H / 32))) : nullptr;
   MOE_CUDA_TRY(mark());
   moe::RouteArgs ra{logits, T, E, k, ids, tw, chunk_hist, L.nchunk, status, 1};
   moe::SortArgs sa{ids, T, E, k, chunk_hist, L.nchunk, counts, offsets, poff, mtb,
@@ -281,11 +288,11 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
     MOE_CUDA_TRY(mark());
   }
   if (x_scale == nullptr) {
-    moe::QuantArgs qa{static_cast<const uint16_t*>(x), T, H, afmt, at(L.xq), at(L.xs), inv_padded, k};
+    moe::QuantArgs qa{static_cast<const uint16_t*>(x), T, H, afmt, at(L.xq), at(L.xs), inv_padded, k, tw, row_w};
     MOE_CUDA_TRY(moe::launch_quant(qa, s));
   } else {
     moe::PermuteArgs pa{static_cast<const uint8_t*>(x), x_scale, T, H, afmt == 0 ? (int64_t)H : (int64_t)H / 2,
-                        inv_padded, k, at(L.xq), at(L.xs)};
+                        inv_padded, k, at(L.xq), at(L.xs), tw, row_w};
     MOE_CUDA_TRY(moe::launch_permute_rows(pa, s));
   }
   MOE_CUDA_TRY(mark());
@@ -365,10 +372,18 @@ moe_status_t forward(const void* x, const uint8_t* x_scale, const float* logits,
   g2.out_codes = nullptr;
   g2.out_sf = nullptr;
   g2.out_bf16 = reinterpret_cast<uint16_t*>(at(L.y2));
+  if (fp8_y2) {
+    g2.epilogue = 3;
+    g2.out_codes = y2q;
+    g2.out_sf = y2s;
+    g2.out_bf16 = nullptr;
+    g2.row_w = row_w;
+  }
   MOE_CUDA_TRY(run_gemm(g2));
   MOE_CUDA_TRY(mark());
 
-  moe::CombineArgs ca{reinterpret_cast<const uint16_t*>(at(L.y2)), tw, inv_padded, T, H, k, static_cast<uint16_t*>(out)};
+  moe::CombineArgs ca{fp8_y2 ? nullptr : reinterpret_cast<const uint16_t*>(at(L.y2)), tw, inv_padded, T, H, k,
+                      static_cast<uint16_t*>(out), y2q, y2s};
   MOE_CUDA_TRY(moe::launch_combine(ca, s));
   MOE_CUDA_TRY(mark());
   return MOE_OK;

@@ -73,6 +73,9 @@ struct QuantArgs {
   // its scales to the 128x4 tile layout.  Canonical mode when inv_padded == null.
   const int32_t* inv_padded;
   int k;
+  // permuted mode, FP8 transport of the GEMM2 rows: row_w[inv_padded[t*k + j]] = topk_w[t*k + j]
+  const float* topk_w;
+  float* row_w;
 };
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
 // Prequantised activations [rows, code_bytes] + canonical scales [rows, K/32] -> padded expert
@@ -87,6 +90,8 @@ struct PermuteArgs {
   int k;
   uint8_t* codes_out;
   uint8_t* scales_out;
+  const float* topk_w;  // with row_w: row_w[inv_padded[q]] = topk_w[q] (as QuantArgs)
+  float* row_w;
 };
 cudaError_t launch_permute_rows(const PermuteArgs& a, cudaStream_t s);
 // bf16 rows h [rows_cap, K] at the padded rows inv_padded[q] of the R routed pairs -> MX codes
@@ -108,7 +113,9 @@ cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8
 struct GemmArgs {
   int act_fmt;            // 0: E4M3 activations (kind::mxf8f6f4), 1: E2M1 (kind::mxf4)
   int epilogue;           // 0: SwiGLU + MX requant (GEMM1), 1: bf16 rows (GEMM2), 2: bf16 SwiGLU
-                          // rows h [rows_cap, N/2] into out_bf16 (GEMM1, bf16-out form)
+                          // rows h [rows_cap, N/2] into out_bf16 (GEMM1, bf16-out form), 3: rows
+                          // weighted by row_w as E4M3 codes [rows_cap, N] in out_codes and one E8M0
+                          // byte per 1x32 block [rows_cap, N/32] in out_sf (GEMM2, FP8 transport)
   const uint8_t* act;     // activation codes [rows_cap, K or K/2]
   const uint8_t* act_sf;  // [rows_cap/128][K/128][512]
   int64_t rows_cap;
@@ -133,6 +140,7 @@ struct GemmArgs {
   uint8_t* act_sf_rot;    // split GEMMs with the wide tail pass: launch_gemm_pair writes the A-scale
                           // atoms of each expert's odd last M tile here, halves swapped, for
                           // launch_gemm_tail_wide (same layout as act_sf); null otherwise
+  const float* row_w;     // epilogue 3: the routing weight of each padded row [rows_cap]
 };
 // Single-CTA GEMMs stage 16 activation rows when T <= 16, and 64 rows (in 64-row work units)
 // when the batch routes at most this many rows per expert on average (T * k <= 16 * E) and the
@@ -260,6 +268,10 @@ struct CombineArgs {
   int64_t T;
   int H, k;
   uint16_t* out;            // bf16 [T, H]
+  // FP8 transport (y2 null): the rows already weighted, as E4M3 codes y2q [rows_cap, H] and one
+  // E8M0 byte per 1x32 block y2s [rows_cap, H/32]; out = bf16(sum over slots of their values)
+  const uint8_t* y2q;
+  const uint8_t* y2s;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 

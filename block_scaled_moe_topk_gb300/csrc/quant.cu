@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(1024) quant_rows_kernel(QuantArgs a) {
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
     if (j < a.k) prow[j] = a.inv_padded[row * a.k + j];
+  if (a.row_w != nullptr && threadIdx.x < a.k)  // FP8 transport: each padded row's routing weight
+    a.row_w[a.inv_padded[row * a.k + threadIdx.x]] = a.topk_w[row * a.k + threadIdx.x];
   float amax = 0.0f;
 #pragma unroll
   for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
@@ -213,6 +215,9 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(PermuteArgs a) {
     for (int j = 0; j < a.k; ++j)
       *reinterpret_cast<uint4*>(a.codes_out + (int64_t)a.inv_padded[t * a.k + j] * row_bytes + c * 16) = v;
   }
+  if (a.row_w != nullptr)  // FP8 transport: each padded row's routing weight
+    for (Idx q = (Idx)blockIdx.x * blockDim.x + threadIdx.x; q < (Idx)a.rows * a.k; q += (Idx)gridDim.x * blockDim.x)
+      a.row_w[a.inv_padded[q]] = a.topk_w[q];
   const Idx nb = (Idx)(a.K / 32);
   const Idx ns = (Idx)a.rows * nb;
   for (Idx i = (Idx)blockIdx.x * blockDim.x + threadIdx.x; i < ns; i += (Idx)gridDim.x * blockDim.x) {

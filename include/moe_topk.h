@@ -114,20 +114,29 @@ typedef enum {
  *                       quantisation, so A2 can differ from the fused epilogue's in a few codes.
  *                       Needs I <= H and I <= 16384 (h is kept in the y2 region), else
  *                       MOE_ERR_UNSUPPORTED_SHAPE.  One kernel more than CHAIN.
+ *   MOE_SCHEDULE_CHAIN_FP8_Y2  the kernel chain with the GEMM2 rows in FP8 transport form ("add
+ *                       A4W4 and FP8 P2P transport support to MegaMoE", Technical Details): GEMM2's
+ *                       epilogue multiplies each row by its routing weight and writes it as E4M3
+ *                       codes with one E8M0 scale per 1x32 block; the combine sums the dequantised
+ *                       rows in fp32 in slot order.  Half the bytes of the bf16 rows, at E4M3
+ *                       precision: the output differs from the other schedules by ~3 % (relative
+ *                       Frobenius error) and matches the FP8-transport form of the layer.  The
+ *                       GEMMs split as in CHAIN; the same number of kernels.
  *   MOE_SCHEDULE_AUTO   the library's choice (every named entry point uses this rule): FUSED
  *                       for T <= 2, and for T <= 16 when I >= 1024 (H <= 16384 in both cases),
  *                       CHAIN otherwise -- the faster of the two on the GB300 over the shapes
  *                       measured (with I = 640 the chain wins from 4-8 tokens on).
  * Every schedule computes the same routing, permutation and quantised activations bit for
- * bit; outputs agree within the parity tolerance of the layer, and each schedule is
- * deterministic (repeated calls give the same bits).
+ * bit; outputs agree within the parity tolerance of the layer (CHAIN_FP8_Y2: of its FP8
+ * transport form), and each schedule is deterministic (repeated calls give the same bits).
  */
 typedef enum {
   MOE_SCHEDULE_AUTO = 0,
   MOE_SCHEDULE_CHAIN = 1,
   MOE_SCHEDULE_FUSED = 2,
   MOE_SCHEDULE_CHAIN_BF16_H = 3,
-  MOE_SCHEDULE_CHAIN_SINGLE_CTA = 4
+  MOE_SCHEDULE_CHAIN_SINGLE_CTA = 4,
+  MOE_SCHEDULE_CHAIN_FP8_Y2 = 5
 } moe_schedule_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -154,6 +163,10 @@ const char* moe_status_string(moe_status_t status);
  *   y2           bf16 [rows_cap, H]        GEMM2 output rows (unweighted; fp32-accumulated,
  *                                          rounded to bf16 like the pages' reduced-precision
  *                                          stage-2 transport)
+ *                MOE_SCHEDULE_CHAIN_FP8_Y2 lays out the same bytes as E4M3 codes of the
+ *                weighted rows [rows_cap, H], then their E8M0 scales [rows_cap, H/32]
+ *                (row-major), then at the next 256-byte boundary each padded row's routing
+ *                weight, fp32 [rows_cap]
  *   sf_rot       u8 [rows_cap/128][max(H, I)/128][512]  scratch of the split GEMMs: the A-scale
  *                atoms of each expert's odd last M tile with their two 64-row halves swapped
  *                (GEMM1's, then GEMM2's); empty unless A8W4 and T * k > 16 * E

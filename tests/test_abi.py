@@ -122,6 +122,9 @@ def test_forward_launch_count():
     assert moe.moe_forward_launch_count_ex(3, *flash, moe.MOE_SCHEDULE_CHAIN_BF16_H) == 6
     assert moe.moe_forward_launch_count_ex(100, *pro, moe.MOE_SCHEDULE_CHAIN_BF16_H) == 8
     assert moe.moe_forward_launch_count_ex(65, *pro, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA) == 7
+    # FP8 transport of the GEMM2 rows: the chain's kernels, its epilogue and combine in FP8 form
+    assert moe.moe_forward_launch_count_ex(65, *pro, moe.MOE_SCHEDULE_CHAIN_FP8_Y2) == 7
+    assert moe.moe_forward_launch_count_ex(3, *flash, moe.MOE_SCHEDULE_CHAIN_FP8_Y2) == 5
 
 
 def test_forward_launch_count_with_split_gemms():
@@ -148,6 +151,8 @@ def test_forward_launch_count_with_split_gemms():
     assert cfg(8192, *pro, 384, 6, a4, auto, True) == 7                      # A4W4
     assert cfg(8192, *pro, 384, 6, a8, moe.MOE_SCHEDULE_CHAIN_SINGLE_CTA, True) == 7
     assert cfg(8192, *pro, 384, 6, a8, moe.MOE_SCHEDULE_CHAIN_BF16_H, True) == 8
+    fp8 = moe.MOE_SCHEDULE_CHAIN_FP8_Y2
+    assert (cfg(8192, *pro, 384, 6, a8, fp8, True), split(8192, *pro, 384, 6, a8, fp8, True)) == (9, 3)
     assert (cfg(1, *pro, 384, 6, a8, auto, True), split(1, *pro, 384, 6, a8, auto, True)) == (1, 0)  # fused
     assert (cfg(0, *pro, 384, 6, a8, auto, True), split(0, *pro, 384, 6, a8, auto, True)) == (0, 0)
     # GEMM2 of H = 384 has a 128-column last N tile: only GEMM1 (N = 2I = 256) splits

@@ -765,3 +765,37 @@ def test_profile_forward_chain_bf16_h():
         torch.cuda.synchronize()
         assert list(us) == list(names) and all(v > 0 for v in us.values())
         assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+# --------------------------------------------------------------------------- FP8 transport of the GEMM2 rows
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("shape,T,prepacked", [("tiny", 40, False), ("tiny", 512, True), ("tiny_wide", 512, True),
+                                               ("tiny_wide", 777, True), ("flash_decode", 300, True)])
+def test_chain_fp8_y2_against_oracle(act, shape, T, prepacked):
+    """GEMM2 rows weighted and written as E4M3 codes with one E8M0 scale per 1x32 block by the
+    GEMM2 epilogue (single-CTA tiles, CTA pairs and the wide tail pass), summed by the FP8
+    combine ("add A4W4 and FP8 P2P transport support to MegaMoE", Technical Details), against
+    the oracle's FP8-transport form: within the parity tolerance and deterministic; against the
+    default form the output moves by E4M3 rounding (a few percent)."""
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 13), synth.gate_logits(T, s.E, 13, skew=s.skew)
+    xd, lgd = x.to(DEV), lg.to(DEV)
+    outs = [torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k, act), dtype=torch.uint8, device=DEV)
+    Wd = W.dev_prepacked() if prepacked else W.dev
+    for o in outs:
+        moe.moe_forward_ex(xd, lgd, *Wd, o, s.E, s.k, ws, act_fmt=act, weight_scales_prepacked=prepacked,
+                           schedule=moe.MOE_SCHEDULE_CHAIN_FP8_Y2)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    toks = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(T).choice(T, 48, replace=False))
+    args = (synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, act)
+    want = oracle.moe_forward(*args, tokens=toks, y2_fp8=True)
+    rel, cos = compare(bits(outs[0])[toks], want)
+    base = oracle.moe_forward(*args, tokens=toks)
+    rel_default, _ = compare(bits(outs[0])[toks], base)
+    print(f"fp8 y2 {shape} T={T} act={act}: rel {rel:.2e} cos {cos:.6f}; against the default form {rel_default:.2e}")
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+    assert rel_default > 4 * rel and rel_default > 5e-3, (rel_default, rel)
