@@ -97,18 +97,33 @@ __global__ void __launch_bounds__(kCombineThreads) combine_fp8_kernel(CombineArg
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j < k) {  // slot order
-        // 2^(s - 127) as an fp32 bit pattern (s = 0: the subnormal 2^-127)
-        const float scale = sb[j] == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb[j] << 23);
         const uint32_t u[2] = {raw[j].x, raw[j].y};
+        if (sb[j] >= 113 && sb[j] <= 142) {
+          // 2^(s - 127) is a normal f16: one mixed-precision FMA per value (the f16 x f16 product is
+          // exact in fp32, so the result equals the fp32 path's: one rounding in the add)
+          const uint16_t sh = (uint16_t)((sb[j] - 112u) << 10);  // f16 bits of 2^(s - 127)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int b = 0; b < 4; b += 2) {  // element 2i in the low byte of each pair
-            const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((u[h] >> (8 * b)) & 0xFFFFu);
-            const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
-            acc[4 * h + b] = fmaf(f.x, scale, acc[4 * h + b]);
-            acc[4 * h + b + 1] = fmaf(f.y, scale, acc[4 * h + b + 1]);
-          }
+            for (int b = 0; b < 4; b += 2) {
+              const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((u[h] >> (8 * b)) & 0xFFFFu);
+              const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+              const uint16_t lo = hr.x, hi = hr.y;
+              asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc[4 * h + b]) : "h"(lo), "h"(sh));
+              asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc[4 * h + b + 1]) : "h"(hi), "h"(sh));
+            }
+        } else {
+          // 2^(s - 127) as an fp32 bit pattern (s = 0: the subnormal 2^-127)
+          const float scale = sb[j] == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb[j] << 23);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int b = 0; b < 4; b += 2) {  // element 2i in the low byte of each pair
+              const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((u[h] >> (8 * b)) & 0xFFFFu);
+              const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
+              acc[4 * h + b] = fmaf(f.x, scale, acc[4 * h + b]);
+              acc[4 * h + b + 1] = fmaf(f.y, scale, acc[4 * h + b + 1]);
+            }
         }
       }
     }

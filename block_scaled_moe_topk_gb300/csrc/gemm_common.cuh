@@ -202,9 +202,10 @@ __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, in
     }
   } else if (EPI == 3) {
     if (!valid) return;  // padding rows: nothing stored
+    // the weight w >= 0 folds into the block maximum and the power-of-two multiplier:
+    // max |w * acc| = w * max |acc| and (w * mult) * acc = (w * acc) * mult in fp32 (exact while
+    // w * acc is a normal fp32 number: rounding is monotone, mult a power of two)
     const float wgt = row_w[prow];
-#pragma unroll
-    for (int i = 0; i < 128; ++i) acc[i] *= wgt;
     const int c0 = nt * kNTile + half * 128;
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {
@@ -212,10 +213,11 @@ __device__ __forceinline__ void store_acc_rows(float (&acc)[128], bool valid, in
       float amax = 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      const MxScale sc = mx_scale<0>(amax);
+      const MxScale sc = mx_scale<0>(amax * wgt);
+      const float m = sc.mult * wgt;
       uint4* dst = reinterpret_cast<uint4*>(out_codes + prow * N + c0 + 32 * blk);
-      const uint2 q0 = pack_e4m3x8(v, sc.mult), q1 = pack_e4m3x8(v + 8, sc.mult);
-      const uint2 q2 = pack_e4m3x8(v + 16, sc.mult), q3 = pack_e4m3x8(v + 24, sc.mult);
+      const uint2 q0 = pack_e4m3x8(v, m), q1 = pack_e4m3x8(v + 8, m);
+      const uint2 q2 = pack_e4m3x8(v + 16, m), q3 = pack_e4m3x8(v + 24, m);
       dst[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
       dst[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
       out_sf[prow * (N / 32) + c0 / 32 + blk] = sc.byte;

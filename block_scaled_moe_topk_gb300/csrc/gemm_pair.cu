@@ -69,7 +69,7 @@ static_assert(kPSfCol0 + kPStagesA * kPSfSlotCols <= kPTmemCols, "pair GEMM TMEM
 // atoms of both rings, the staging buffers, the barriers and the pair-tile prefix.
 template <int EPI>
 struct PairGeo {
-  static constexpr bool kOutStaging = EPI == 1;
+  static constexpr bool kOutStaging = EPI == 1 || EPI == 3;  // GEMM2 rows: bf16, or FP8 transport codes
   static constexpr int kStagesW = kOutStaging ? 7 : 8;
   static constexpr int kWOff = kPStagesA * kPABytes;              // the weight ring after the activation ring
   static constexpr int kSfaOff = kWOff + kStagesW * kPBBytes;     // activation-scale atoms, 512 B a slot
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);  // registers hold the tile
       acc_phase ^= 1u;
-      if (G::kOutStaging && __all_sync(0xffffffffu, valid)) {
+      if (EPI == 1 && G::kOutStaging && __all_sync(0xffffffffu, valid)) {
         // GEMM2 rows as bf16 (nearest even) through shared memory when all 32 rows of this warp
         // are routed rows: each 32-column chunk leaves as one TMA store (as in gemm.cu)
         const uint32_t buf = sbase + G::kOutOff + (uint32_t)(warp - 2) * kPOutStageBytes;
@@ -426,6 +426,47 @@ __global__ void __launch_bounds__(kPThreads, 1) moe_gemm_pair_kernel(const __gri
             bulk_commit_group();
           }
         }
+      } else if (EPI == 3 && G::kOutStaging && __all_sync(0xffffffffu, valid)) {
+        // FP8 transport: the weighted row's four 32-column blocks as E4M3 codes, staged like the
+        // bf16 rows (32 rows x 64 bytes a chunk, 64-byte swizzle, one TMA store), two chunks; the
+        // four scale bytes of the row leave as one 4-byte store
+        const uint32_t buf = sbase + G::kOutOff + (uint32_t)(warp - 2) * kPOutStageBytes;
+        const int x0 = pt.nt * kNTile + half * 128;
+        const int y0 = (int)(prow - lane);
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+        // the routing weight w >= 0 folds into the block maximum and the quantiser's power-of-two
+        // multiplier: max |w * acc| = w * max |acc| and (w * mult) * acc = (w * acc) * mult in fp32
+        // (exact while w * acc is a normal fp32 number: rounding is monotone, mult a power of two)
+        const float wgt = p.row_w[prow];
+        uint32_t sbytes = 0;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float mult[2];  // the chunk's two 32-column blocks, times w
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(acc[64 * c + 32 * bb + i]));
+            const MxScale sc = mx_scale<0>(amax * wgt);
+            mult[bb] = sc.mult * wgt;
+            sbytes |= (uint32_t)sc.byte << (8 * (2 * c + bb));
+          }
+          if (lane == 0) bulk_wait_read_all();  // the previous store has read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // 16 columns a chunk piece: block 2c + i/2
+            const float* v = acc + 64 * c + 16 * i;
+            const uint2 q0 = pack_e4m3x8(v, mult[i / 2]), q1 = pack_e4m3x8(v + 8, mult[i / 2]);
+            st_shared_v4(buf + (uint32_t)lane * 64u + (((uint32_t)i ^ swz) << 4), q0.x, q0.y, q1.x, q1.y);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmap_out, buf, x0 + 64 * c, y0);
+            bulk_commit_group();
+          }
+        }
+        *reinterpret_cast<uint32_t*>(p.out_sf + prow * (p.N / 32) + x0 / 32) = sbytes;
       } else {
         store_acc_rows<ACT, EPI>(acc, valid, prow, pt.nt, half, p.N, p.out_codes, p.out_sf, p.out_bf16, p.row_w);
       }
@@ -537,6 +578,16 @@ cudaError_t launch_pair_typed(const GemmArgs& a, cudaStream_t s) {
     const cuuint32_t box[2] = {32, 32};
     const cuuint32_t es[2] = {1, 1};
     if (encode(&p.tmap_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_bf16, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (EPI == 3) {  // FP8 transport codes [rows_cap, N] bytes, box 64 bytes x 32 rows
+    const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.rows_cap};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.N};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&p.tmap_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.out_codes, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
