@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_kernel(QuantArgs a) {
         dst[1] = c1;
         if (scale_writer) a.scales[row * (K / 32) + kb] = sc.byte;
       } else {  // workspace rows (256-byte aligned, K % 32 == 0): one 16-byte store per row
+        if (col0 == 0 && a.row_w != nullptr)  // FP8 transport: each padded row's routing weight
+          for (int j = 0; j < a.k; ++j) a.row_w[a.inv_padded[row * a.k + j]] = a.topk_w[row * a.k + j];
         const uint4 c = make_uint4(c0.x, c0.y, c1.x, c1.y);
         for (int j = 0; j < a.k; ++j) {
           const int64_t prow = a.inv_padded[row * a.k + j];
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_kernel(QuantArgs a) {
         *reinterpret_cast<uint2*>(a.codes + row * (K / 2) + col0 / 2) = c;
         if (scale_writer) a.scales[row * (K / 32) + kb] = sc.byte;
       } else {
+        if (col0 == 0 && a.row_w != nullptr)
+          for (int j = 0; j < a.k; ++j) a.row_w[a.inv_padded[row * a.k + j]] = a.topk_w[row * a.k + j];
         for (int j = 0; j < a.k; ++j) {
           const int64_t prow = a.inv_padded[row * a.k + j];
           *reinterpret_cast<uint2*>(a.codes + prow * (K / 2) + col0 / 2) = c;

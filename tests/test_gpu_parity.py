@@ -799,3 +799,22 @@ def test_chain_fp8_y2_against_oracle(act, shape, T, prepacked):
     print(f"fp8 y2 {shape} T={T} act={act}: rel {rel:.2e} cos {cos:.6f}; against the default form {rel_default:.2e}")
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
     assert rel_default > 4 * rel and rel_default > 5e-3, (rel_default, rel)
+
+
+@pytest.mark.parametrize("schedule", [moe.MOE_SCHEDULE_CHAIN, moe.MOE_SCHEDULE_CHAIN_FP8_Y2])
+def test_wide_rows_against_oracle(schedule):
+    """H > 16384: the forward's quantiser runs its grid-stride form (a token row no longer fits one
+    block), which also records the routing weight of each padded row for the FP8 transport."""
+    E, k, H, I, T = 8, 2, 16896, 128, 70
+    W = Weights(E, H, I, seed=0, device=DEV)
+    x, lg = synth.x_bf16(T, H, 17), synth.gate_logits(T, E, 17)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_workspace_bytes(T, H, I, E, k), dtype=torch.uint8, device=DEV)
+    moe.moe_forward_ex(x.to(DEV), lg.to(DEV), *W.dev, out, E, k, ws, schedule=schedule)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    toks = np.arange(0, T, 5)
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, moe.MOE_ACT_MXFP8, tokens=toks,
+                              y2_fp8=schedule == moe.MOE_SCHEDULE_CHAIN_FP8_Y2)
+    rel, cos = compare(bits(out)[toks], want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
