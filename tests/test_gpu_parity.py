@@ -818,3 +818,19 @@ def test_wide_rows_against_oracle(schedule):
                               y2_fp8=schedule == moe.MOE_SCHEDULE_CHAIN_FP8_Y2)
     rel, cos = compare(bits(out)[toks], want)
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_MXFP4])
+@pytest.mark.parametrize("shape,T", [("tiny", 40), ("tiny", 512), ("tiny_wide", 512)])
+def test_chain_fp8_y2_prequant_against_oracle(act, shape, T):
+    """The FP8 transport with prequantised input (the oracle's own codes of x, prepacked weight
+    scales): the permuting copy records each padded row's routing weight for the GEMM2 epilogue."""
+    s = synth.SHAPES[shape]
+    W = Weights(s.E, s.H, s.I, seed=0, device=DEV, from_bf16=True) if shape == "tiny" else _weights(s)
+    x, lg = synth.x_bf16(T, s.H, 19), synth.gate_logits(T, s.E, 19, skew=s.skew)
+    out, ws = _run_forward(act, x, lg, W, s.E, s.k, entry="ex", schedule=moe.MOE_SCHEDULE_CHAIN_FP8_Y2)
+    assert moe.moe_read_device_status(ws) == 0
+    toks = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(T).choice(T, 48, replace=False))
+    want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, act, tokens=toks, y2_fp8=True)
+    rel, cos = compare(bits(out)[toks], want)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
