@@ -610,6 +610,14 @@ def test_forward_hidden_size_not_a_multiple_of_256(act, H, I, T):
                        weight_scales_prepacked=True)
     torch.cuda.synchronize()
     assert torch.equal(out_p.view(torch.int16), out.view(torch.int16))
+    # the FP8 transport of the GEMM2 rows stores the 128-column last tile's codes and scales too
+    out_f = torch.empty_like(out)
+    moe.moe_forward_ex(x.to(DEV), lg.to(DEV), w1, _prepack(w1s), w2, _prepack(w2s), out_f, E, k, ws, act_fmt=act,
+                       weight_scales_prepacked=True, schedule=moe.MOE_SCHEDULE_CHAIN_FP8_Y2)
+    torch.cuda.synchronize()
+    want_f = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, E, k, act, y2_fp8=True)
+    rel, cos = compare(bits(out_f), want_f)
+    assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
 
 
 @pytest.mark.parametrize("shape,T", [("flash_tp2", 1), ("flash_tp2", 96), ("draft_tp4", 3), ("draft_tp4", 500)])
