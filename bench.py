@@ -271,8 +271,9 @@ def run_ours(args):
     x, lg = make_workload(T, rank, dev, E)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     if args.quick:  # a few plain forwards (for profiler captures of a small case)
+        sched = {"auto": moe.MOE_SCHEDULE_AUTO, "fp8_y2": moe.MOE_SCHEDULE_CHAIN_FP8_Y2}[args.schedule]
         for _ in range(args.warmup + args.steps):
-            fwd(x, lg, *W, out, E, k, ws)
+            moe.moe_forward_ex(x, lg, *W, out, E, k, ws, weight_scales_prepacked=True, schedule=sched)
         torch.cuda.synchronize()
         clocks.stop()
         print(json.dumps({"quick": True, "T": T, "E": E, "status": moe.moe_read_device_status(ws)}))
@@ -636,6 +637,8 @@ def main():
                     help="expert count (smaller values only for profiler captures of a small case)")
     ap.add_argument("--quick", action="store_true", help="only W+K plain forwards, no report (profiling)")
     ap.add_argument("--quick-extras", action="store_true", help="skip the A4W4 and per-config sweeps")
+    ap.add_argument("--schedule", choices=["auto", "fp8_y2"], default="auto",
+                    help="with --quick: the forwards' schedule (fp8_y2: the FP8 transport of the GEMM2 rows)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="V4-Pro tokens of the all-core oracle sample")

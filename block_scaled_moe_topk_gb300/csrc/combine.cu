@@ -68,9 +68,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
 // FP8 transport: the k rows of a token arrive already weighted, as E4M3 codes with one E8M0
 // scale per 32 columns; out = bf16_rne(sum over slots of code value * 2^(scale - 127)), fp32 in
 // slot order.  Each thread owns 8 consecutive columns: one 8-byte code load and one scale byte
-// per slot.  The kernel is bound by the decode arithmetic, not by its (halved) bytes: the
-// hardware pair conversion E4M3 -> f16 is the cheapest decode measured (an integer decode,
-// sign and bits placed into an fp32 and rescaled, took 1.5x as long).
+// per slot.  The decode decides the speed: the hardware pair conversion E4M3 -> f16, then one
+// mixed-precision FMA per value into the fp32 sum (below); with f16 -> f32 conversions in between
+// the kernel was slower than the bf16 combine despite half the bytes, and an integer decode (sign
+// and bits placed into an fp32 and rescaled) slower still.  It then runs at ~60 % of DRAM
+// bandwidth with the ALU pipe ~60 % busy.
 template <typename Idx>
 __global__ void __launch_bounds__(kCombineThreads) combine_fp8_kernel(CombineArgs a) {
   const int H = a.H, k = a.k;
