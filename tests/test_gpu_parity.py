@@ -842,3 +842,28 @@ def test_chain_fp8_y2_prequant_against_oracle(act, shape, T):
     want = oracle.moe_forward(synth.bf16_bits(x), lg.numpy(), *W.host, s.E, s.k, act, tokens=toks, y2_fp8=True)
     rel, cos = compare(bits(out)[toks], want)
     assert rel <= TOL_REL and cos >= TOL_COS, (rel, cos)
+
+
+def test_profile_forward_chain_fp8_y2():
+    """Per-kernel timing of the FP8 transport schedule: the chain's kernel names, and the same
+    output bits as the forward without events (small and large batch)."""
+    s = synth.SHAPES["tiny_wide"]
+    W = _weights(s)
+    for T, names in ((40, moe.KERNEL_NAMES_SMALL), (512, None)):
+        x, lg = synth.x_bf16(T, s.H, 0).to(DEV), synth.gate_logits(T, s.E, 0).to(DEV)
+        out_a = torch.empty(T, s.H, dtype=torch.bfloat16, device=DEV)
+        out_b = torch.empty_like(out_a)
+        ws = torch.empty(moe.moe_workspace_bytes(T, s.H, s.I, s.E, s.k), dtype=torch.uint8, device=DEV)
+        Wp = W.dev_prepacked()
+        moe.moe_forward_ex(x, lg, *Wp, out_a, s.E, s.k, ws, weight_scales_prepacked=True,
+                           schedule=moe.MOE_SCHEDULE_CHAIN_FP8_Y2)
+        us = moe.moe_profile_forward(moe.MOE_ACT_MXFP8, x, lg, *Wp, out_b, s.E, s.k, ws, prepacked_scales=True,
+                                     schedule=moe.MOE_SCHEDULE_CHAIN_FP8_Y2)
+        torch.cuda.synchronize()
+        if names is not None:
+            assert list(us) == list(names)
+        else:  # both GEMMs split into the pair kernel and the wide tail pass
+            assert list(us) == ["route", "scan", "scatter", "quant", "gemm1_pairs", "gemm1_tails", "gemm2_pairs",
+                                "gemm2_tails", "combine"]
+        assert all(v > 0 for v in us.values())
+        assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
